@@ -1,0 +1,79 @@
+"""Pins of the oracle's Medusa heads and top-k (Medusa Heads glossary page,
+"How heads predict later tokens")."""
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import oracle as O
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_zero_init_heads_reproduce_lm_head_exactly(dtype):
+    # The page's check: W1 and b1 start at zero and W2 is a copy of lm_head, so
+    # every head prints True against lm_head's own logits (hidden 256, vocab
+    # 1000, 3 heads, h ~ N(0,1)).  z = h + SiLU(0) = h exactly, so the float64
+    # logits must be bitwise equal.
+    x = W.heads_inputs(seed=1, B=1, H=256, V=1000, K=3, dtype=dtype, zero_init=True)
+    heads = O.heads_logits(x["h"], x["w1"], x["b1"], x["w2"], dtype)
+    lm = O.lm_head_logits(x["h"], x["lm_head"], dtype)
+    assert [bool(np.array_equal(heads[:, k], lm)) for k in range(3)] == [True, True, True]
+
+
+def _numpy_heads(h, w1, b1, w2):
+    # Library restatement on float64 arrays: W2 (h + silu(W1 h + b1)).
+    u = np.einsum("kij,bj->bki", w1, h) + b1[None]
+    z = h[:, None, :] + u / (1.0 + np.exp(-u))
+    return np.einsum("kvi,bki->bkv", w2, z), z
+
+
+def test_heads_match_numpy_restatement_fp32():
+    rng = np.random.default_rng(0)
+    B, K, H, V = 3, 2, 24, 37
+    h = rng.standard_normal((B, H)).astype(np.float32)
+    w1 = (rng.standard_normal((K, H, H)) * 0.3).astype(np.float32)  # not symmetric
+    b1 = rng.standard_normal((K, H)).astype(np.float32)              # nonzero bias
+    w2 = rng.standard_normal((K, V, H)).astype(np.float32)
+    got, z = O.heads_logits(h, w1, b1, w2, "f32", return_z=True)
+    ref, zr = _numpy_heads(*(a.astype(np.float64) for a in (h, w1, b1, w2)))
+    np.testing.assert_allclose(z, zr, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-11)
+
+
+def test_heads_bf16_decoding_is_exact():
+    rng = np.random.default_rng(1)
+    B, K, H, V = 2, 2, 16, 9
+    h32 = rng.standard_normal((B, H)).astype(np.float32)
+    w1 = rng.standard_normal((K, H, H)).astype(np.float32) * 0.2
+    b1 = rng.standard_normal((K, H)).astype(np.float32)
+    w2 = rng.standard_normal((K, V, H)).astype(np.float32)
+    bits = [W.f32_to_bf16_bits(a) for a in (h32, w1, b1, w2)]
+    got = O.heads_logits(*bits, "bf16")
+    ref, _ = _numpy_heads(*(W.bf16_bits_to_f32(b).astype(np.float64) for b in bits))
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-11)
+
+
+def test_silu_limits():
+    # large |u|: SiLU(u) -> u for u >> 0 and -> 0 for u << 0 (no NaN from exp overflow)
+    H = 2
+    h = np.zeros((1, H), np.float32)
+    w1 = np.zeros((1, H, H), np.float32)
+    b1 = np.array([[800.0, -800.0]], np.float32)
+    w2 = np.eye(H, dtype=np.float32)[None]
+    got, z = O.heads_logits(h, w1, b1, w2, "f32", return_z=True)
+    assert z[0, 0, 0] == 800.0 and z[0, 0, 1] == 0.0 and np.isfinite(got).all()
+
+
+def test_topk_matches_stable_sort_with_ties():
+    rng = np.random.default_rng(2)
+    x = rng.integers(-5, 6, size=(7, 300)).astype(np.float64)  # many exact ties
+    idx, val = O.topk(x, 9)
+    for r in range(x.shape[0]):
+        order = np.lexsort((np.arange(x.shape[1]), -x[r]))[:9]  # value desc, index asc
+        assert idx[r].tolist() == order.tolist()
+        assert val[r].tolist() == x[r, order].tolist()
+
+
+def test_topk_k_equals_n_is_a_permutation():
+    x = np.array([[3.0, 1.0, 3.0, 2.0]])
+    idx, _ = O.topk(x, 4)
+    assert idx[0].tolist() == [0, 2, 3, 1]
