@@ -1,0 +1,469 @@
+"""Benchmark of one Medusa decode step on GB300.
+
+Workload: the Vicuna-7B-shaped batch-1 step (hidden 4096, vocab 32000, 5 heads,
+top-8 per head, 64-node sparse tree, 32 query heads x 128 head dim, KV length
+2048, bf16 storage, greedy acceptance with planted alpha = 0.8, then KV
+compaction), with seeded synthetic inputs and random-init weights of that shape.
+
+A step is one pass of the whole hot path through the C ABI:
+  medusa_heads_topk -> medusa_build_tree -> medusa_tree_attention (one layer)
+  -> medusa_verify_accept_tree -> medusa_kv_compact
+with every input resident in HBM.  The step reads ~1.52 GB, more than L2, so
+consecutive steps start cold.  kv_len is restored before each step (compaction
+grows it) so every step sees the same workload.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same step instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+CFG = W.CONFIGS[2]
+METRIC = "Medusa decode steps/s (tree tokens verified/s = steps/s x 64 nodes)"
+WORKLOAD = ("vicuna7b-shaped medusa step, batch 1: hidden 4096, vocab 32000, 5 heads, top-8, "
+            "sparse 64-node tree, 32x128 attention over KV 2048 (one layer), greedy acceptance, "
+            "KV compaction; bf16 storage, fp32 accumulate")
+
+# DRAM bytes per launch of the heads call, from the ncu capture summarised in
+# profiles/ (dram__bytes_read.sum + dram__bytes_write.sum summed over its three
+# kernels), with the sha1 of heads.cu it was taken on; null once that file changes.
+HEADS_TRAFFIC = {"sha1": None, "bytes": None}
+
+
+def _sha1(path):
+    with open(path, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _tree_tables():
+    import medusa_speculative_decoding_gb300 as M
+    paths = M.sparse_tree_paths(64, 5, 8, 0.6, 0.5)
+    return M.tree_layout(paths, 5)
+
+
+def make_inputs(seed=2):
+    c = CFG
+    t = _tree_tables()
+    N = t["N"]
+    heads = W.heads_inputs(seed, c["B"], c["H"], c["V"], c["K"], c["dtype"])
+    kv_len = W.kv_lengths(seed, c["B"], c["L_lo"], c["L_hi"])
+    Lmax = c["L_hi"] + N
+    att = W.attention_inputs(seed, c["B"], N, c["Hq"], c["Hkv"], c["D"], Lmax, c["dtype"])
+    ht = W.hidden_tree(seed, c["B"], N, c["H"], c["dtype"])
+    root = W.root_tokens(seed, c["B"], c["V"])
+    return dict(tree=t, heads=heads, kv_len=kv_len, Lmax=Lmax, att=att, ht=ht, root=root)
+
+
+def algorithmic_bytes(c, N, Lmax_used):
+    K, H, V, B = c["K"], c["H"], c["V"], c["B"]
+    heads = K * (H * H + H + V * H) * 2 + B * H * 2 + B * K * c["topk"] * 8
+    att = 2 * c["Hkv"] * Lmax_used * c["D"] * 2 * B + B * N * c["Hq"] * c["D"] * (2 + 4)
+    verify = B * N * c["V"] * 4 + B * N * 4
+    return heads, att, verify
+
+
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed loop runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+class Step:
+    """Device buffers and the five C-ABI calls of one decode step."""
+
+    def __init__(self, inp, device):
+        import torch
+        import medusa_speculative_decoding_gb300 as M
+        self.M, self.torch = M, torch
+        c = CFG
+        t = inp["tree"]
+        self.t = t
+        self.N, self.Dmax = t["N"], t["max_depth"]
+        dev = device
+
+        def td(a):
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+            if a.dtype == np.uint64:
+                return torch.from_numpy(a.view(np.int64)).to(dev)
+            return torch.from_numpy(a).to(dev)
+
+        self.td = td
+        hd = inp["heads"]
+        self.h, self.w1, self.b1, self.w2 = (td(hd[k]) for k in ("h", "w1", "b1", "w2"))
+        self.root = td(inp["root"])
+        self.depth, self.rank, self.parent = td(t["depth"]), td(t["rank"]), td(t["parent"])
+        self.mask = td(t["mask"])
+        self.q = td(inp["att"]["q"])
+        self.kc, self.vc = td(inp["att"]["k_cache"]), td(inp["att"]["v_cache"])
+        self.kv_len0 = td(inp["kv_len"])
+        self.kv_len = self.kv_len0.clone()
+        self.ht = td(inp["ht"])
+        B, K, topk, V = c["B"], c["K"], c["topk"], c["V"]
+        i32 = torch.int32
+        self.idx = torch.empty((B, K, topk), dtype=i32, device=dev)
+        self.val = torch.empty((B, K, topk), dtype=torch.float32, device=dev)
+        self.cand = torch.empty((B, self.N), dtype=i32, device=dev)
+        self.att_out = torch.empty((B, self.N, c["Hq"], c["D"]), dtype=torch.float32, device=dev)
+        self.acc = dict(accept_len=torch.empty(B, dtype=i32, device=dev),
+                        best_node=torch.empty(B, dtype=i32, device=dev),
+                        path_nodes=torch.empty((B, self.Dmax + 1), dtype=i32, device=dev),
+                        next_tok=torch.empty(B, dtype=i32, device=dev))
+        self.h_next = torch.empty((B, c["H"]), dtype=torch.bfloat16, device=dev)
+        self.src = torch.empty((B, self.Dmax + 1), dtype=i32, device=dev)
+        u8 = torch.uint8
+        self.ws_heads = torch.empty(max(16, M.heads_topk_workspace(B, K, c["H"], V, topk)), dtype=u8, device=dev)
+        self.ws_att_n = M.tree_attention_workspace(B, self.N, c["Hq"], c["Hkv"], c["D"], inp["Lmax"])
+        self.ws_att = torch.empty(max(16, self.ws_att_n), dtype=u8, device=dev)
+        self.ws_ver = torch.empty(max(16, M.verify_accept_workspace(B, self.N, V)), dtype=u8, device=dev)
+        # verifier logits planted around this step's own candidates (setup, untimed)
+        self.heads()
+        self.M.build_tree(self.idx, self.root, self.depth, self.rank, out=self.cand)
+        cand = self.cand.cpu().numpy()
+        self.vlogits = td(W.planted_logits(2, cand, t["parent"], V, c["alpha"]))
+        self.launches = 3 + 1 + (2 if self.ws_att_n > 0 else 1) + 2 + 2
+
+    def heads(self):
+        c = CFG
+        self.M.heads_topk(self.h, self.w1, self.b1, self.w2, c["topk"], out=(self.idx, self.val, None),
+                          ws=self.ws_heads)
+
+    def run(self, ev=None):
+        M = self.M
+        self.kv_len.copy_(self.kv_len0)
+        if ev is not None:
+            ev[0].record()
+        self.heads()
+        if ev is not None:
+            ev[1].record()
+        M.build_tree(self.idx, self.root, self.depth, self.rank, out=self.cand)
+        if ev is not None:
+            ev[2].record()
+        M.tree_attention(self.q, self.kc, self.vc, self.kv_len, self.mask, out=self.att_out, ws=self.ws_att)
+        if ev is not None:
+            ev[3].record()
+        M.verify_accept_tree(self.vlogits, self.cand, self.parent, self.depth, self.Dmax, out=self.acc,
+                             ws=self.ws_ver)
+        M.kv_compact(self.kc, self.vc, self.kv_len, self.acc["path_nodes"], self.acc["accept_len"],
+                     self.acc["best_node"], self.N, self.Dmax, hidden_tree=self.ht, h_next=self.h_next,
+                     src_idx=self.src)
+
+
+def run_e2e(step, steps, warmup):
+    """Same step through the C ABI with host buffers: per-step inputs copied from
+    pinned host memory, results read back, all inside the timed region."""
+    torch = step.torch
+    c = CFG
+    pin = lambda t: t.cpu().pin_memory()
+    L = int(step.kv_len0[0].item())
+    N = step.N
+    host = dict(h=pin(step.h), q=pin(step.q), vl=pin(step.vlogits), ht=pin(step.ht),
+                tk=pin(step.kc[:, :, L:L + N].contiguous()), tv=pin(step.vc[:, :, L:L + N].contiguous()))
+    outs = [step.acc["accept_len"], step.acc["best_node"], step.acc["path_nodes"],
+            step.acc["next_tok"], step.h_next]
+    host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def one():
+        step.h.copy_(host["h"], non_blocking=True)
+        step.q.copy_(host["q"], non_blocking=True)
+        step.vlogits.copy_(host["vl"], non_blocking=True)
+        step.ht.copy_(host["ht"], non_blocking=True)
+        step.kc[:, :, L:L + N].copy_(host["tk"], non_blocking=True)
+        step.vc[:, :, L:L + N].copy_(host["tv"], non_blocking=True)
+        step.run()
+        for o, ho in zip(outs, host_out):
+            ho.copy_(o, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    return dt, h2d, d2h
+
+
+# ----------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# ----------------------------------------------------------------------------
+class OracleSample:
+    """Times the CPU oracle on a bounded sample of the step and scales each
+    component to the full step: heads of one head restricted to nv vocab rows
+    (its W1 in full), R attention query rows, the full verify and compaction."""
+
+    def __init__(self, inp, nv, R):
+        from oracle import oracle as O
+        self.O = O
+        self.inp = inp
+        self.nv, self.R = nv, R
+        c = CFG
+        self.t = t = O.tree_layout(O.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5)
+        self.N = t["N"]
+        rng = np.random.default_rng(0)
+        self.rows = np.stack([np.zeros(R, int), rng.integers(0, self.N, R), rng.integers(0, c["Hq"], R)],
+                             1).astype(np.int32)
+        self.cand = O.build_tree(W.random_topk_lists(2, c["B"], c["K"], c["topk"], c["V"]), inp["root"],
+                                 t["depth"], t["rank"])
+        self.vlogits = W.planted_logits(2, self.cand, t["parent"], c["V"], c["alpha"])
+        self.hd = inp["heads"]
+
+    def step(self, k):
+        """One sample step; returns the scaled full-step seconds."""
+        O, c, t = self.O, CFG, self.t
+        K, H, V, nv = c["K"], c["H"], c["V"], self.nv
+        hd = self.hd
+        k = k % K
+        t0 = time.perf_counter()
+        O.heads_logits(hd["h"], hd["w1"][k:k + 1], hd["b1"][k:k + 1], hd["w2"][k:k + 1, :nv], c["dtype"])
+        t1 = time.perf_counter()
+        O.tree_attention(self.inp["att"]["q"], self.inp["att"]["k_cache"], self.inp["att"]["v_cache"],
+                         self.inp["kv_len"], t["mask"], c["dtype"], 1 / np.sqrt(c["D"]), rows=self.rows)
+        t2 = time.perf_counter()
+        r = O.verify_tree(self.vlogits, self.cand, t["parent"], t["depth"], t["max_depth"])
+        t3 = time.perf_counter()
+        O.kv_compact(self.inp["att"]["k_cache"], self.inp["att"]["v_cache"], self.inp["kv_len"],
+                     r["path_nodes"], r["accept_len"], r["best_node"], self.inp["ht"], self.N, t["max_depth"])
+        t4 = time.perf_counter()
+        heads_scale = K * (H * H + V * H) / (H * H + nv * H)
+        att_scale = c["B"] * self.N * c["Hq"] / self.R
+        return (t1 - t0) * heads_scale + (t2 - t1) * att_scale + (t3 - t2) + (t4 - t3)
+
+
+def oracle_cores():
+    return 1  # the oracle is single-threaded C
+
+
+def cpu_baseline(inp):
+    s = OracleSample(inp, nv=CFG["V"], R=256)
+    secs = [s.step(k) for k in range(2)]
+    est = statistics.mean(secs)
+    return {"value": 1.0 / est, "unit": "steps/s", "cores": oracle_cores(), "kind": "oracle",
+            "sample": "2 sample steps: one head in full (W1 and all 32000 W2 rows), 256 of 2048 "
+                      "attention query rows, full greedy verify and compaction; each component "
+                      "scaled to the full step; single-threaded float64 C"}
+
+
+# ----------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        inp = make_inputs_host_only()
+        budget = 150.0 / (args.steps + args.warmup)
+        nv, R = (1024, 16) if budget > 0.08 else (128, 4)
+        s = OracleSample(inp, nv=nv, R=R)
+        for k in range(args.warmup):
+            s.step(k)
+        t0 = time.perf_counter()
+        est = [s.step(k) for k in range(args.steps)]
+        wall = time.perf_counter() - t0
+        T = statistics.mean(est)
+        val = 1.0 / T
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "steps/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": T * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": WORKLOAD, "sample_wall_s": wall},
+                "cpu_baseline": {"value": val, "unit": "steps/s", "cores": oracle_cores(), "kind": "oracle",
+                                 "sample": f"per step: one head with {nv} of 32000 W2 rows (W1 in full), "
+                                           f"{R} of 2048 attention query rows, full verify and "
+                                           "compaction; each component scaled to the full step"},
+                "e2e": {"value": val, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from medusa_speculative_decoding_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+
+    inp = make_inputs()
+    step = Step(inp, dev)
+    c = CFG
+    N = step.N
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        step.run(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    heads_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(K))
+    att_ms = statistics.mean(evs[i][2].elapsed_time(evs[i][3]) for i in range(K))
+    ms_step = ms_total / K
+    value = world * K / (ms_total / 1e3)
+
+    e2e_s, h2d, d2h = run_e2e(step, max(20, K // 4), args.warmup)
+    e2e_val = world * max(20, K // 4) / e2e_s
+
+    peak, peak_kind = _peaks()
+    hb, ab, vb = algorithmic_bytes(c, N, int(inp["kv_len"][0]) + N)
+    heads_gbs = hb / (heads_ms * 1e-3) / 1e9
+    att_gbs = ab / (att_ms * 1e-3) / 1e9
+    cur = _sha1(os.path.join(ROOT, "medusa_speculative_decoding_gb300", "csrc", "heads.cu"))
+    traffic = HEADS_TRAFFIC["bytes"] if HEADS_TRAFFIC["sha1"] == cur else None
+
+    line = {"metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": c["B"] * world, "tree_nodes": N,
+                       "kv_len": int(inp["kv_len"][0]), "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: each step streams 1.52 GB",
+                       "tree_tokens_verified_per_s": value * N * c["B"]},
+            "roofline": {"bound": "hbm", "kernel": "medusa_heads_topk (W1+SiLU, W2+top-k, merge)",
+                         "achieved": heads_gbs, "peak": peak, "unit": "GB/s", "frac": heads_gbs / peak,
+                         "traffic": traffic, "peak_kind": peak_kind, "algorithmic_bytes": hb,
+                         "ms": heads_ms},
+            "attention": {"achieved": att_gbs, "unit": "GB/s", "frac": att_gbs / peak,
+                          "algorithmic_bytes": ab, "ms": att_ms},
+            "clocks": clocks,
+            "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": step.launches * K}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def make_inputs_host_only(seed=2):
+    """Inputs of the reference arm: the same generator, tree from the oracle."""
+    from oracle import oracle as O
+    c = CFG
+    t = O.tree_layout(O.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5)
+    N = t["N"]
+    heads = W.heads_inputs(seed, c["B"], c["H"], c["V"], c["K"], c["dtype"])
+    kv_len = W.kv_lengths(seed, c["B"], c["L_lo"], c["L_hi"])
+    Lmax = c["L_hi"] + N
+    att = W.attention_inputs(seed, c["B"], N, c["Hq"], c["Hkv"], c["D"], Lmax, c["dtype"])
+    ht = W.hidden_tree(seed, c["B"], N, c["H"], c["dtype"])
+    root = W.root_tokens(seed, c["B"], c["V"])
+    return dict(tree=t, heads=heads, kv_len=kv_len, Lmax=Lmax, att=att, ht=ht, root=root)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

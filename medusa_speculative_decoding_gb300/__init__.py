@@ -1,0 +1,19 @@
+"""GB300 (sm_103a) hot path of the Medusa decode step.
+
+The computation lives in libmedusa_gb300.so (hand-written CUDA kernels behind
+the C ABI of include/medusa.h); this package is its thin Python binding:
+
+  heads_topk          Medusa heads h + SiLU(W1 h + b1) -> W2, per-head top-k
+  sparse_tree_paths   the most accurate rank tuples (host)
+  tree_layout         node table, ancestor mask and paths of a tree (host)
+  build_tree          candidate tokens of the tree nodes
+  tree_attention      ancestor-masked attention of all candidates in one pass
+  verify_accept_tree  greedy / typical acceptance, longest accepted branch
+  verify_accept_chain speculative-sampling acceptance with k + 1 tokens
+  kv_compact          keep the accepted branch's KV rows and hidden state
+"""
+from ._native import MedusaError, lib  # noqa: F401
+from .api import (build_tree, heads_topk, heads_topk_workspace, kv_compact,  # noqa: F401
+                  sparse_tree_paths, tree_attention, tree_attention_workspace, tree_layout,
+                  verify_accept_chain, verify_accept_tree, verify_accept_workspace,
+                  verify_chain_workspace)

@@ -1,0 +1,69 @@
+// common.cu -- status messages and cached device properties.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace medusa {
+
+static thread_local char g_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int check_launch(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(MEDUSA_ERR_CUDA, "%s: kernel launch failed: %s", what, cudaGetErrorString(e));
+    return MEDUSA_OK;
+}
+
+namespace {
+constexpr int kMaxDev = 64;
+int g_sms[kMaxDev];
+int g_smem[kMaxDev];
+std::mutex g_mu;
+
+int current_dev() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDev) return 0;
+    return d;
+}
+}  // namespace
+
+int sm_count() {
+    int d = current_dev();
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sms[d] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || v <= 0)
+            v = 148;
+        g_sms[d] = v;
+    }
+    return g_sms[d];
+}
+
+int max_smem_optin() {
+    int d = current_dev();
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_smem[d] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) != cudaSuccess ||
+            v <= 0)
+            v = 48 * 1024;
+        g_smem[d] = v;
+    }
+    return g_smem[d];
+}
+
+}  // namespace medusa
+
+extern "C" const char* medusa_last_error(void) { return medusa::g_msg; }
+extern "C" int medusa_abi_version(void) { return 1; }

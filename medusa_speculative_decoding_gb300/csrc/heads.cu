@@ -1,0 +1,376 @@
+// heads.cu -- Medusa heads and per-head top-k ("Medusa Heads" glossary page,
+// "How heads predict later tokens": head k reads the last hidden state h and
+// scores position t + k + 1 through one residual SiLU layer and a vocab
+// projection).
+//
+// At decode batch sizes (B <= 8) both products are matrix-vector products over
+// weights that are read once per step, so the heads are bound by HBM bandwidth:
+//   K1 heads_w1_silu : z[b,k,:] = h[b] + SiLU(W1_k h[b] + b1_k)   (float32 z)
+//   K2 heads_w2_topk : logits = W2_k z, streamed over vocab slices; each CTA keeps
+//                      its slice's logits in shared memory and emits its top-k
+//   K3 topk_merge    : merges the per-slice lists into the final sorted top-k
+// Each warp walks R weight rows at once with 16-byte loads (lanes stride over
+// the hidden dimension); the vectors z / h live in shared memory as float32 and
+// are read once per R rows.
+#include <float.h>
+#include <limits.h>
+
+#include "common.cuh"
+
+namespace medusa {
+namespace {
+
+constexpr int kRows = 4;    // weight rows a warp reduces together
+constexpr int kUnroll = 2;  // 16-byte chunks per row in flight per lane
+
+template <typename WT>
+struct Elems { static constexpr int n = 16 / sizeof(WT); };
+
+template <typename WT>
+__device__ __forceinline__ float load_scalar(const WT* p, size_t i);
+template <>
+__device__ __forceinline__ float load_scalar<float>(const float* p, size_t i) { return p[i]; }
+template <>
+__device__ __forceinline__ float load_scalar<uint16_t>(const uint16_t* p, size_t i) {
+    return bf16_to_f32(p[i]);
+}
+
+// acc += dot(16-byte weight chunk, x[0..n))
+template <typename WT>
+__device__ __forceinline__ float dot_chunk(const uint4& w, const float* x, float acc);
+template <>
+__device__ __forceinline__ float dot_chunk<uint16_t>(const uint4& w, const float* x, float acc) {
+    const float4 a = *reinterpret_cast<const float4*>(x);
+    const float4 b = *reinterpret_cast<const float4*>(x + 4);
+    acc = fmaf(bf16_lo(w.x), a.x, acc);
+    acc = fmaf(bf16_hi(w.x), a.y, acc);
+    acc = fmaf(bf16_lo(w.y), a.z, acc);
+    acc = fmaf(bf16_hi(w.y), a.w, acc);
+    acc = fmaf(bf16_lo(w.z), b.x, acc);
+    acc = fmaf(bf16_hi(w.z), b.y, acc);
+    acc = fmaf(bf16_lo(w.w), b.z, acc);
+    acc = fmaf(bf16_hi(w.w), b.w, acc);
+    return acc;
+}
+template <>
+__device__ __forceinline__ float dot_chunk<float>(const uint4& w, const float* x, float acc) {
+    const float4 a = *reinterpret_cast<const float4*>(x);
+    acc = fmaf(__uint_as_float(w.x), a.x, acc);
+    acc = fmaf(__uint_as_float(w.y), a.y, acc);
+    acc = fmaf(__uint_as_float(w.z), a.z, acc);
+    acc = fmaf(__uint_as_float(w.w), a.w, acc);
+    return acc;
+}
+
+// Partial dot products of rows row0..row0+kRows-1 of W ([rows][H]) with the NB
+// shared-memory vectors xs[b*H ..].  Rows past last_row repeat last_row (their
+// results are discarded by the caller).  Each lane covers chunks lane, lane+32..
+template <typename WT, int NB>
+__device__ __forceinline__ void dot_rows(const WT* __restrict__ W, int row0, int last_row, int H,
+                                         const float* __restrict__ xs, float (&acc)[kRows][NB],
+                                         int lane) {
+    constexpr int VEC = Elems<WT>::n;
+    const int nchunk = H / VEC;
+    const char* rp[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+        int row = min(row0 + r, last_row);
+        rp[r] = reinterpret_cast<const char*>(W + (size_t)row * H);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
+    }
+    for (int c0 = lane; c0 < nchunk; c0 += 32 * kUnroll) {
+        uint4 w[kUnroll][kRows];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int c = c0 + 32 * u;
+#pragma unroll
+            for (int r = 0; r < kRows; ++r)
+                w[u][r] = c < nchunk ? ld_stream16(rp[r] + (size_t)c * 16) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int c = c0 + 32 * u;
+            if (c < nchunk) {
+                const float* xc = xs + (size_t)c * VEC;
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+#pragma unroll
+                    for (int r = 0; r < kRows; ++r)
+                        acc[r][b] = dot_chunk<WT>(w[u][r], xc + (size_t)b * H, acc[r][b]);
+            }
+        }
+    }
+}
+
+template <typename WT>
+__device__ __forceinline__ void load_vector_to_smem(const WT* src, float* dst, int n) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = load_scalar<WT>(src, i);
+}
+
+// K1: z[b,k,i] = h[b,i] + SiLU(sum_j W1[k,i,j] h[b,j] + b1[k,i])
+template <typename WT, int NB, int THREADS>
+__global__ void __launch_bounds__(THREADS) heads_w1_silu_kernel(
+    const WT* __restrict__ h, const WT* __restrict__ w1, const WT* __restrict__ b1, int K, int H,
+    int rows_per_cta, float* __restrict__ z) {
+    extern __shared__ __align__(16) float xs[];  // [NB][H]
+    const int k = blockIdx.y;
+    const int row_begin = blockIdx.x * rows_per_cta;
+    const int row_end = min(H, row_begin + rows_per_cta);
+    load_vector_to_smem<WT>(h, xs, NB * H);
+    __syncthreads();
+    if (row_begin >= row_end) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const WT* wk = w1 + (size_t)k * H * H;
+    for (int g = row_begin + warp * kRows; g < row_end; g += (THREADS / 32) * kRows) {
+        float acc[kRows][NB];
+        dot_rows<WT, NB>(wk, g, row_end - 1, H, xs, acc, lane);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float s = warp_sum(acc[r][b]);
+                const int i = g + r;
+                if (i < row_end && lane == ((r * NB + b) & 31)) {
+                    const float u = s + load_scalar<WT>(b1, (size_t)k * H + i);
+                    const float silu = u / (1.f + expf(-u));
+                    z[((size_t)b * K + k) * H + i] = xs[(size_t)b * H + i] + silu;
+                }
+            }
+    }
+}
+
+// Selects, in `passes` rounds, the best remaining (value, index) pair among
+// n entries given by get(j) -> (value, index); one warp.  Writes through put().
+template <typename Get, typename Put>
+__device__ __forceinline__ void warp_select_topk(int n, int passes, Get get, Put put, int lane) {
+    float lastv = INFINITY;
+    int lasti = -1;
+    for (int t = 0; t < passes; ++t) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        for (int j = lane; j < n; j += 32) {
+            float x;
+            int xi;
+            get(j, x, xi);
+            if (better(lastv, lasti, x, xi) && better(x, xi, bv, bi)) { bv = x; bi = xi; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        }
+        if (lane == 0) put(t, bv, bi);
+        lastv = bv;
+        lasti = bi;
+    }
+}
+
+// K2: logits of one vocab slice of head k, then the slice's top-k per sequence.
+template <typename WT, int NB, int THREADS>
+__global__ void __launch_bounds__(THREADS) heads_w2_topk_kernel(
+    const WT* __restrict__ w2, const float* __restrict__ z, int K, int H, int V, int rows_per_cta,
+    int topk, float* __restrict__ logits, float* __restrict__ cval, int* __restrict__ cidx) {
+    extern __shared__ __align__(16) float sm[];
+    float* xs = sm;                       // [NB][H]
+    float* lg = sm + (size_t)NB * H;      // [NB][rows_per_cta]
+    const int s = blockIdx.x, S = gridDim.x, k = blockIdx.y;
+    const int v0 = s * rows_per_cta;
+    const int v1 = min(V, v0 + rows_per_cta);
+    for (int i = threadIdx.x; i < NB * H; i += THREADS) {
+        const int b = i / H, j = i - b * H;
+        xs[i] = z[((size_t)b * K + k) * H + j];
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const WT* wk = w2 + (size_t)k * V * H;
+    for (int g = v0 + warp * kRows; g < v1; g += (THREADS / 32) * kRows) {
+        float acc[kRows][NB];
+        dot_rows<WT, NB>(wk, g, v1 - 1, H, xs, acc, lane);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float sum = warp_sum(acc[r][b]);
+                const int v = g + r;
+                if (v < v1 && lane == ((r * NB + b) & 31)) {
+                    lg[(size_t)b * rows_per_cta + (v - v0)] = sum;
+                    if (logits) logits[((size_t)b * K + k) * V + v] = sum;
+                }
+            }
+    }
+    __syncthreads();
+    const int n = v1 - v0;
+    for (int b = warp; b < NB; b += THREADS / 32) {
+        const float* row = lg + (size_t)b * rows_per_cta;
+        float* ov = cval + (((size_t)b * K + k) * S + s) * topk;
+        int* oi = cidx + (((size_t)b * K + k) * S + s) * topk;
+        warp_select_topk(
+            n, topk, [&](int j, float& x, int& xi) { x = row[j]; xi = v0 + j; },
+            [&](int t, float v, int i) { ov[t] = v; oi[t] = i; }, lane);
+    }
+}
+
+// K3: merge the S per-slice lists of each (b, k) into the sorted top-k.
+__global__ void __launch_bounds__(32) topk_merge_kernel(const float* __restrict__ cval,
+                                                         const int* __restrict__ cidx, int K, int S,
+                                                         int topk, int32_t* __restrict__ topk_idx,
+                                                         float* __restrict__ topk_val) {
+    const int k = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
+    const size_t base = ((size_t)b * K + k) * S * topk;
+    int32_t* oi = topk_idx + ((size_t)b * K + k) * topk;
+    float* ov = topk_val ? topk_val + ((size_t)b * K + k) * topk : nullptr;
+    warp_select_topk(
+        S * topk, topk, [&](int j, float& x, int& xi) { x = cval[base + j]; xi = cidx[base + j]; },
+        [&](int t, float v, int i) {
+            oi[t] = i;
+            if (ov) ov[t] = v;
+        },
+        lane);
+}
+
+struct HeadsPlan {
+    int threads;       // 256 or 512
+    int rows1;         // K1 rows per CTA
+    int grid1;         // K1 CTAs per head
+    int rows2;         // K2 vocab rows per CTA
+    int S;             // K2 slices per head
+    size_t smem1, smem2;
+    size_t off_z, off_val, off_idx, ws_bytes;
+};
+
+HeadsPlan plan_heads(int B, int K, int H, int V, int topk) {
+    HeadsPlan p{};
+    const size_t xbytes = (size_t)B * H * sizeof(float);
+    const bool big = xbytes > 64 * 1024;
+    p.threads = big ? 512 : 256;
+    const int per_sm = big ? 1 : 2;
+    const int target = sm_count() * per_sm;
+    // K1: whole warp-row groups per CTA
+    const int grp = (p.threads / 32) * kRows;
+    int r1 = (int)(((long long)H * K + target - 1) / target);
+    p.rows1 = ((r1 + grp - 1) / grp) * grp;
+    p.grid1 = (H + p.rows1 - 1) / p.rows1;
+    // K2: vocab slices so that K * S fills one wave; each slice >= topk rows
+    int s0 = target / K;
+    if (s0 < 1) s0 = 1;
+    int r2 = (V + s0 - 1) / s0;
+    // a slice's logits live in shared memory next to the vectors
+    const long long room = ((long long)max_smem_optin() - 1024 - (long long)xbytes) / ((long long)B * 4);
+    if (room > 0 && r2 > room) r2 = (int)room;
+    if (r2 < topk) r2 = topk;
+    p.rows2 = r2;
+    p.S = (V + r2 - 1) / r2;
+    p.smem1 = xbytes;
+    p.smem2 = xbytes + (size_t)B * r2 * sizeof(float);
+    size_t off = 0;
+    p.off_z = off;
+    off = align_up(off + (size_t)B * K * H * sizeof(float), 256);
+    p.off_val = off;
+    off = align_up(off + (size_t)B * K * p.S * topk * sizeof(float), 256);
+    p.off_idx = off;
+    off = align_up(off + (size_t)B * K * p.S * topk * sizeof(int), 256);
+    p.ws_bytes = off;
+    return p;
+}
+
+template <typename WT, int NB, int THREADS>
+int launch_heads(const void* h, const void* w1, const void* b1, const void* w2, int K, int H, int V,
+                 int topk, int32_t* topk_idx, float* topk_val, float* logits, char* ws,
+                 const HeadsPlan& p, cudaStream_t st) {
+    float* z = reinterpret_cast<float*>(ws + p.off_z);
+    float* cval = reinterpret_cast<float*>(ws + p.off_val);
+    int* cidx = reinterpret_cast<int*>(ws + p.off_idx);
+    auto k1 = heads_w1_silu_kernel<WT, NB, THREADS>;
+    auto k2 = heads_w2_topk_kernel<WT, NB, THREADS>;
+    if (p.smem1 > 48 * 1024)
+        cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem1);
+    if (p.smem2 > 48 * 1024)
+        cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem2);
+    k1<<<dim3(p.grid1, K), THREADS, p.smem1, st>>>(static_cast<const WT*>(h),
+                                                   static_cast<const WT*>(w1),
+                                                   static_cast<const WT*>(b1), K, H, p.rows1, z);
+    int rc = check_launch("heads_w1_silu");
+    if (rc) return rc;
+    k2<<<dim3(p.S, K), THREADS, p.smem2, st>>>(static_cast<const WT*>(w2), z, K, H, V, p.rows2,
+                                               topk, logits, cval, cidx);
+    rc = check_launch("heads_w2_topk");
+    if (rc) return rc;
+    topk_merge_kernel<<<dim3(K, NB), 32, 0, st>>>(cval, cidx, K, p.S, topk, topk_idx, topk_val);
+    return check_launch("topk_merge");
+}
+
+template <typename WT, int NB>
+int dispatch_threads(const void* h, const void* w1, const void* b1, const void* w2, int K, int H,
+                     int V, int topk, int32_t* ti, float* tv, float* lg, char* ws,
+                     const HeadsPlan& p, cudaStream_t st) {
+    if (p.threads == 512)
+        return launch_heads<WT, NB, 512>(h, w1, b1, w2, K, H, V, topk, ti, tv, lg, ws, p, st);
+    return launch_heads<WT, NB, 256>(h, w1, b1, w2, K, H, V, topk, ti, tv, lg, ws, p, st);
+}
+
+template <typename WT>
+int dispatch_batch(int B, const void* h, const void* w1, const void* b1, const void* w2, int K,
+                   int H, int V, int topk, int32_t* ti, float* tv, float* lg, char* ws,
+                   const HeadsPlan& p, cudaStream_t st) {
+    switch (B) {
+#define MEDUSA_CASE(n) \
+    case n: return dispatch_threads<WT, n>(h, w1, b1, w2, K, H, V, topk, ti, tv, lg, ws, p, st);
+        MEDUSA_CASE(1) MEDUSA_CASE(2) MEDUSA_CASE(3) MEDUSA_CASE(4)
+        MEDUSA_CASE(5) MEDUSA_CASE(6) MEDUSA_CASE(7) MEDUSA_CASE(8)
+#undef MEDUSA_CASE
+    }
+    return fail(MEDUSA_ERR_UNSUPPORTED, "heads_topk: batch %d not in [1, 8]", B);
+}
+
+int check_heads_shapes(int B, int K, int H, int V, int topk) {
+    if (B < 1 || K < 1 || H < 1 || V < 1 || topk < 1)
+        return fail(MEDUSA_ERR_INVALID_ARG, "heads_topk: sizes must be positive (B=%d K=%d H=%d V=%d topk=%d)",
+                    B, K, H, V, topk);
+    if (B > 8 || K > 64 || H < 8 || H > 16384 || H % 8 || (long long)B * H > 49152 || topk > 16 ||
+        topk > V)
+        return fail(MEDUSA_ERR_UNSUPPORTED,
+                    "heads_topk: unsupported shape (B=%d K=%d H=%d V=%d topk=%d): need B<=8, K<=64, "
+                    "8<=H<=16384, H%%8==0, B*H<=49152, topk<=16, topk<=V",
+                    B, K, H, V, topk);
+    return MEDUSA_OK;
+}
+
+}  // namespace
+}  // namespace medusa
+
+using namespace medusa;
+
+extern "C" size_t medusa_heads_topk_workspace(int B, int K, int H, int V, int topk) {
+    if (check_heads_shapes(B, K, H, V, topk)) return 0;
+    return plan_heads(B, K, H, V, topk).ws_bytes;
+}
+
+extern "C" int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void* w2,
+                                 medusa_dtype dtype, int B, int K, int H, int V, int topk,
+                                 int32_t* topk_idx, float* topk_val, float* logits, void* ws,
+                                 size_t ws_bytes, void* stream) {
+    int rc = check_heads_shapes(B, K, H, V, topk);
+    if (rc) return rc;
+    if (!h || !w1 || !b1 || !w2 || !topk_idx)
+        return fail(MEDUSA_ERR_INVALID_ARG, "heads_topk: null input or output pointer");
+    if (!aligned16(w1) || !aligned16(w2))
+        return fail(MEDUSA_ERR_INVALID_ARG, "heads_topk: w1 and w2 must be 16-byte aligned");
+    if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "heads_topk: unknown dtype %d", (int)dtype);
+    HeadsPlan p = plan_heads(B, K, H, V, topk);
+    if (!ws || ws_bytes < p.ws_bytes)
+        return fail(MEDUSA_ERR_WORKSPACE, "heads_topk: workspace of %zu bytes needed, %zu given",
+                    p.ws_bytes, ws ? ws_bytes : (size_t)0);
+    if (!aligned16(ws)) return fail(MEDUSA_ERR_INVALID_ARG, "heads_topk: ws must be 16-byte aligned");
+    if (p.smem2 > (size_t)max_smem_optin())
+        return fail(MEDUSA_ERR_UNSUPPORTED, "heads_topk: %zu bytes of shared memory needed", p.smem2);
+    cudaStream_t st = as_stream(stream);
+    char* w = static_cast<char*>(ws);
+    if (dtype == MEDUSA_BF16)
+        return dispatch_batch<uint16_t>(B, h, w1, b1, w2, K, H, V, topk, topk_idx, topk_val, logits,
+                                        w, p, st);
+    return dispatch_batch<float>(B, h, w1, b1, w2, K, H, V, topk, topk_idx, topk_val, logits, w, p,
+                                 st);
+}

@@ -1,0 +1,453 @@
+// verify.cu -- acceptance of candidates.
+//
+// Tree ("Medusa Heads" glossary page, "Tree attention and acceptance"): greedy
+// decoding accepts a candidate that equals the model's top choice; typical
+// acceptance keeps a candidate whose base-model probability clears a threshold
+// tied to the entropy of the distribution; the longest accepted branch is kept.
+//   row_stats_kernel   : one pass over each verifier-logits chunk (HBM-bound):
+//                        argmax, and for typical acceptance the running
+//                        (max, sum exp, sum exp * x) of x = logit / T
+//   accept_tree_kernel : per sequence: merge chunk stats, test each candidate
+//                        against its parent's row, AND along ancestors, pick the
+//                        deepest accepted node (lowest index on ties)
+//
+// Chain (speculative-decoding e-book page, "Faster without changing the
+// result"; "Why a round always yields exactly k + 1 tokens"): accept draft x
+// with probability min(1, p(x)/q(x)); at the first rejection draw from
+// max(0, p - q) normalised; if all are accepted draw a bonus token from the
+// next p.
+//   chain_scan_kernel   : finds the first rejection of its sequence, then runs
+//                         the exponential race over one vocab chunk of the row
+//                         to draw from
+//   chain_finish_kernel : merges the chunk winners and writes the k + 1 tokens
+#include <float.h>
+#include <limits.h>
+
+#include "common.cuh"
+
+namespace medusa {
+namespace {
+
+constexpr int kChunk = 4096;     // vocab entries per stats CTA
+constexpr int kStatThreads = 256;
+
+struct RowStat {      // per (row, chunk)
+    float maxv;       // largest logit
+    int arg;          // its lowest index
+    float m, s, a;    // x = logit/T: max, sum e^(x-m), sum e^(x-m) (x-m)
+    float pad[3];
+};
+
+// merge softmax/entropy partial states (m, s, a)
+__device__ __forceinline__ void merge_msa(float& m, float& s, float& a, float m2, float s2,
+                                          float a2) {
+    if (s2 == 0.f) return;
+    if (s == 0.f) { m = m2; s = s2; a = a2; return; }
+    const float mn = fmaxf(m, m2);
+    const float c1 = expf(m - mn), c2 = expf(m2 - mn);
+    a = c1 * (a + (m - mn) * s) + c2 * (a2 + (m2 - mn) * s2);
+    s = c1 * s + c2 * s2;
+    m = mn;
+}
+
+template <bool TYPICAL>
+__global__ void __launch_bounds__(kStatThreads) row_stats_kernel(const float* __restrict__ logits,
+                                                                 int V, int nchunk, float inv_t,
+                                                                 RowStat* __restrict__ stats) {
+    const int c = blockIdx.x, row = blockIdx.y;
+    const float* x = logits + (size_t)row * V;
+    const int v0 = c * kChunk, v1 = min(V, v0 + kChunk);
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    float m = -INFINITY, s = 0.f, a = 0.f;
+    auto take = [&](float l, int v) {
+        if (better(l, v, bv, bi)) { bv = l; bi = v; }
+        if (TYPICAL) {
+            const float xv = l * inv_t;
+            if (!(xv > -INFINITY)) return;  // contributes no probability mass
+            if (s == 0.f) {
+                m = xv;
+                s = 1.f;
+                a = 0.f;
+            } else if (xv > m) {
+                const float c1 = expf(m - xv);
+                a = c1 * (a + (m - xv) * s);
+                s = c1 * s + 1.f;
+                m = xv;
+            } else {
+                const float e = expf(xv - m);
+                s += e;
+                a += e * (xv - m);
+            }
+        }
+    };
+    // vectorised body when the row start is 16-byte aligned
+    const bool vec = ((reinterpret_cast<uintptr_t>(x + v0) & 15u) == 0);
+    int v = v0;
+    if (vec) {
+        const int nv = (v1 - v0) / 4;
+        const float4* x4 = reinterpret_cast<const float4*>(x + v0);
+        for (int i = threadIdx.x; i < nv; i += kStatThreads) {
+            const uint4 r = ld_stream16(x4 + i);
+            const int base = v0 + 4 * i;
+            take(__uint_as_float(r.x), base);
+            take(__uint_as_float(r.y), base + 1);
+            take(__uint_as_float(r.z), base + 2);
+            take(__uint_as_float(r.w), base + 3);
+        }
+        v = v0 + 4 * nv;
+    }
+    for (int i = v + threadIdx.x; i < v1; i += kStatThreads) take(x[i], i);
+    // block reduction
+    __shared__ float sv[kStatThreads / 32], sm_[kStatThreads / 32], ss[kStatThreads / 32],
+        sa[kStatThreads / 32];
+    __shared__ int si[kStatThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        if (TYPICAL) {
+            const float om = __shfl_xor_sync(0xffffffffu, m, o);
+            const float os = __shfl_xor_sync(0xffffffffu, s, o);
+            const float oa = __shfl_xor_sync(0xffffffffu, a, o);
+            merge_msa(m, s, a, om, os, oa);
+        }
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) { sv[warp] = bv; si[warp] = bi; sm_[warp] = m; ss[warp] = s; sa[warp] = a; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kStatThreads / 32; ++w) {
+            if (better(sv[w], si[w], bv, bi)) { bv = sv[w]; bi = si[w]; }
+            if (TYPICAL) merge_msa(m, s, a, sm_[w], ss[w], sa[w]);
+        }
+        RowStat r;
+        r.maxv = bv; r.arg = bi; r.m = m; r.s = s; r.a = a;
+        r.pad[0] = r.pad[1] = r.pad[2] = 0.f;
+        stats[(size_t)row * nchunk + c] = r;
+    }
+}
+
+constexpr int kAcceptThreads = 512;  // >= max nodes
+
+template <bool TYPICAL>
+__global__ void __launch_bounds__(kAcceptThreads) accept_tree_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ cand,
+    const int32_t* __restrict__ parent, const int32_t* __restrict__ depth, int N, int V, int Dmax,
+    int nchunk, float inv_t, float eps, float delta, const RowStat* __restrict__ stats,
+    int32_t* __restrict__ accept_len, int32_t* __restrict__ best_node,
+    int32_t* __restrict__ path_nodes, int32_t* __restrict__ next_tok) {
+    __shared__ int s_arg[kAcceptThreads];
+    __shared__ float s_m[kAcceptThreads], s_s[kAcceptThreads], s_tau[kAcceptThreads];
+    __shared__ unsigned char s_pass[kAcceptThreads];
+    __shared__ int s_best;
+    const int b = blockIdx.x;
+    const int u = threadIdx.x;
+    if (u < N) {
+        const RowStat* st = stats + ((size_t)b * N + u) * nchunk;
+        float bv = -INFINITY, m = -INFINITY, s = 0.f, a = 0.f;
+        int bi = INT_MAX;
+        for (int c = 0; c < nchunk; ++c) {
+            const RowStat r = st[c];
+            if (better(r.maxv, r.arg, bv, bi)) { bv = r.maxv; bi = r.arg; }
+            if (TYPICAL) merge_msa(m, s, a, r.m, r.s, r.a);
+        }
+        s_arg[u] = bi;
+        if (TYPICAL) {
+            // H = -sum P ln P = ln s - a / s  (x relative to m);  tau = min(eps, delta e^-H)
+            const float H = logf(s) - a / s;
+            s_m[u] = m;
+            s_s[u] = s;
+            s_tau[u] = fminf(eps, delta * expf(-H));
+        }
+    }
+    if (threadIdx.x == 0) s_best = 1023;  // node 0 (the root) unless a deeper node wins
+    __syncthreads();
+    // candidate tests against the parent's row
+    if (u < N) {
+        bool pass = true;
+        if (u > 0) {
+            const int pu = parent[u];
+            const int tok = cand[(size_t)b * N + u];
+            if (pu < 0 || pu >= u || tok < 0 || tok >= V) {
+                pass = false;
+            } else if (TYPICAL) {
+                const float x = logits[((size_t)b * N + pu) * V + tok] * inv_t;
+                const float P = expf(x - s_m[pu]) / s_s[pu];
+                pass = P > s_tau[pu];
+            } else {
+                pass = tok == s_arg[pu];
+            }
+        }
+        s_pass[u] = pass;
+    }
+    __syncthreads();
+    // accepted iff every node on the path to the root passes; the key orders
+    // nodes by (depth, -index)
+    if (u < N) {
+        // a node that passes has a valid parent index below its own, so the walk
+        // strictly descends and ends at the root
+        bool acc = true;
+        int a_ = u;
+        while (a_ > 0) {
+            if (!s_pass[a_]) { acc = false; break; }
+            a_ = parent[a_];
+        }
+        if (acc) atomicMax(&s_best, min(max(depth[u], 0), 1 << 20) * 1024 + (1023 - u));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int best = 1023 - (s_best & 1023);
+        const int d = depth[best];
+        accept_len[b] = d;
+        best_node[b] = best;
+        next_tok[b] = s_arg[best];
+        int32_t* path = path_nodes + (size_t)b * (Dmax + 1);
+        for (int e = 0; e <= Dmax; ++e) path[e] = -1;
+        int a_ = best;  // every node on this path passed, so its parents are valid
+        while (a_ >= 0) {
+            const int da = depth[a_];
+            if (da >= 0 && da <= Dmax) path[da] = a_;
+            a_ = a_ > 0 ? parent[a_] : -1;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// SplitMix64 (Steele, Lea and Flood, 2014)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t sm64(uint64_t state, uint64_t n) {
+    uint64_t z = state + n * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+__device__ __forceinline__ uint64_t row_key(uint64_t seed, uint64_t stream, uint64_t b,
+                                            uint64_t round, uint64_t pos) {
+    uint64_t x = sm64(seed, 1);
+    x = sm64(x ^ stream, 1);
+    x = sm64(x ^ b, 1);
+    x = sm64(x ^ round, 1);
+    return sm64(x ^ pos, 1);
+}
+__device__ __forceinline__ float u24(uint64_t h) { return (float)(h >> 40) * (1.0f / 16777216.0f); }
+__device__ __forceinline__ float u24p(uint64_t h) {
+    return (float)((h >> 40) + 1) * (1.0f / 16777216.0f);
+}
+
+constexpr int kChainThreads = 256;
+constexpr int kChainChunk = 8192;
+
+struct ChainPart {  // per (sequence, chunk)
+    float key;      // best race key
+    int tok;        // its token
+    float pmax;     // fallback: best p and its token
+    int pidx;
+};
+
+// First rejected position (1-based) of sequence b, or gamma + 1 if none.
+__device__ int first_reject(const float* p, const float* q, const int32_t* draft, int gamma, int V,
+                            int b, uint64_t seed, uint64_t round) {
+    __shared__ int s_first;
+    if (threadIdx.x == 0) s_first = gamma + 1;
+    __syncthreads();
+    for (int i = threadIdx.x; i < gamma; i += blockDim.x) {
+        const int x = draft[(size_t)b * gamma + i];
+        bool accept = false;
+        if (x >= 0 && x < V) {
+            const float qi = q[((size_t)b * gamma + i) * V + x];
+            const float pi = p[((size_t)b * (gamma + 1) + i) * V + x];
+            const float u = u24(sm64(row_key(seed, 1, b, round, i + 1), 1));
+            // sign of u*q - p with one rounding: equals the sign of the exact value
+            accept = fmaf(u, qi, -pi) < 0.f;
+        }
+        if (!accept) atomicMin(&s_first, i + 1);
+    }
+    __syncthreads();
+    return s_first;
+}
+
+__global__ void __launch_bounds__(kChainThreads) chain_scan_kernel(
+    const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ draft,
+    int gamma, int V, int nchunk, uint64_t seed, uint64_t round, ChainPart* __restrict__ parts,
+    int* __restrict__ firsts) {
+    const int c = blockIdx.x, b = blockIdx.y;
+    const int first = first_reject(p, q, draft, gamma, V, b, seed, round);
+    if (c == 0 && threadIdx.x == 0) firsts[b] = first;
+    const bool bonus = first > gamma;
+    const int pos = bonus ? gamma + 1 : first;          // 1-based position drawn at
+    const float* pr = p + ((size_t)b * (gamma + 1) + (pos - 1)) * V;
+    const float* qr = bonus ? nullptr : q + ((size_t)b * gamma + (pos - 1)) * V;
+    const uint64_t key = row_key(seed, bonus ? 3 : 2, b, round, pos);
+    const int v0 = c * kChainChunk, v1 = min(V, v0 + kChainChunk);
+    float bk = INFINITY, pm = -INFINITY;
+    int bt = INT_MAX, pi = INT_MAX;
+    for (int v = v0 + threadIdx.x; v < v1; v += kChainThreads) {
+        const float pv = pr[v];
+        if (better(pv, v, pm, pi)) { pm = pv; pi = v; }
+        const float w = bonus ? pv : pv - qr[v];
+        if (w > 0.f) {
+            const float k = -logf(u24p(sm64(key, (uint64_t)v + 1))) / w;
+            if (k < bk || (k == bk && v < bt)) { bk = k; bt = v; }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        const int ot = __shfl_xor_sync(0xffffffffu, bt, o);
+        if (ok < bk || (ok == bk && ot < bt)) { bk = ok; bt = ot; }
+        const float op = __shfl_xor_sync(0xffffffffu, pm, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, pi, o);
+        if (better(op, oi, pm, pi)) { pm = op; pi = oi; }
+    }
+    __shared__ ChainPart sp[kChainThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) sp[warp] = ChainPart{bk, bt, pm, pi};
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ChainPart r = sp[0];
+        for (int w = 1; w < kChainThreads / 32; ++w) {
+            const ChainPart o = sp[w];
+            if (o.key < r.key || (o.key == r.key && o.tok < r.tok)) { r.key = o.key; r.tok = o.tok; }
+            if (better(o.pmax, o.pidx, r.pmax, r.pidx)) { r.pmax = o.pmax; r.pidx = o.pidx; }
+        }
+        parts[(size_t)b * nchunk + c] = r;
+    }
+}
+
+__global__ void __launch_bounds__(32) chain_finish_kernel(const ChainPart* __restrict__ parts,
+                                                          const int* __restrict__ firsts,
+                                                          const int32_t* __restrict__ draft,
+                                                          int gamma, int nchunk,
+                                                          int32_t* __restrict__ n_acc,
+                                                          int32_t* __restrict__ out_tok) {
+    const int b = blockIdx.x, lane = threadIdx.x;
+    float bk = INFINITY, pm = -INFINITY;
+    int bt = INT_MAX, pi = INT_MAX;
+    for (int c = lane; c < nchunk; c += 32) {
+        const ChainPart r = parts[(size_t)b * nchunk + c];
+        if (r.key < bk || (r.key == bk && r.tok < bt)) { bk = r.key; bt = r.tok; }
+        if (better(r.pmax, r.pidx, pm, pi)) { pm = r.pmax; pi = r.pidx; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        const int ot = __shfl_xor_sync(0xffffffffu, bt, o);
+        if (ok < bk || (ok == bk && ot < bt)) { bk = ok; bt = ot; }
+        const float op = __shfl_xor_sync(0xffffffffu, pm, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, pi, o);
+        if (better(op, oi, pm, pi)) { pm = op; pi = oi; }
+    }
+    const int k = firsts[b] - 1;  // accepted drafts
+    const int tok = bt != INT_MAX ? bt : pi;
+    for (int e = lane; e <= gamma; e += 32)
+        out_tok[(size_t)b * (gamma + 1) + e] = e < k ? draft[(size_t)b * gamma + e] : (e == k ? tok : -1);
+    if (lane == 0) n_acc[b] = k;
+}
+
+struct ChainPlan {
+    int nchunk;
+    size_t off_parts, off_first, ws_bytes;
+};
+ChainPlan plan_chain(int B, int V) {
+    ChainPlan p{};
+    p.nchunk = (V + kChainChunk - 1) / kChainChunk;
+    p.off_parts = 0;
+    p.off_first = align_up((size_t)B * p.nchunk * sizeof(ChainPart), 256);
+    p.ws_bytes = align_up(p.off_first + (size_t)B * sizeof(int), 256);
+    return p;
+}
+
+size_t verify_ws(int B, int N, int V) {
+    const int nchunk = (V + kChunk - 1) / kChunk;
+    return align_up((size_t)B * N * nchunk * sizeof(RowStat), 256);
+}
+
+}  // namespace
+}  // namespace medusa
+
+using namespace medusa;
+
+extern "C" size_t medusa_verify_accept_workspace(int B, int N, int V) {
+    if (B < 1 || N < 1 || V < 1) return 0;
+    return verify_ws(B, N, V);
+}
+
+extern "C" int medusa_verify_accept_tree(const float* logits, const int32_t* cand,
+                                         const int32_t* parent, const int32_t* depth, int B, int N,
+                                         int V, int Dmax, medusa_accept_mode mode,
+                                         float temperature, float eps, float delta,
+                                         int32_t* accept_len, int32_t* best_node,
+                                         int32_t* path_nodes, int32_t* next_tok, void* ws,
+                                         size_t ws_bytes, void* stream) {
+    if (!logits || !cand || !parent || !depth || !accept_len || !best_node || !path_nodes ||
+        !next_tok)
+        return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_tree: null pointer");
+    if (B < 1 || N < 1 || V < 1 || Dmax < 0)
+        return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_tree: bad sizes");
+    if (N > kAcceptThreads || B > 65535)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "verify_accept_tree: N=%d above %d", N, kAcceptThreads);
+    if (mode != MEDUSA_ACCEPT_GREEDY && mode != MEDUSA_ACCEPT_TYPICAL)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "verify_accept_tree: unknown mode %d", (int)mode);
+    if (mode == MEDUSA_ACCEPT_TYPICAL && !(temperature > 0.f))
+        return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_tree: temperature must be > 0");
+    const size_t need = verify_ws(B, N, V);
+    if (!ws || ws_bytes < need)
+        return fail(MEDUSA_ERR_WORKSPACE, "verify_accept_tree: workspace of %zu bytes needed, %zu given",
+                    need, ws ? ws_bytes : (size_t)0);
+    if (!aligned16(ws)) return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_tree: ws must be 16-byte aligned");
+    const int nchunk = (V + kChunk - 1) / kChunk;
+    if ((long long)B * N > 65535)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "verify_accept_tree: B*N above 65535");
+    RowStat* stats = static_cast<RowStat*>(ws);
+    cudaStream_t st = as_stream(stream);
+    const float inv_t = 1.f / temperature;
+    dim3 g1(nchunk, B * N);
+    if (mode == MEDUSA_ACCEPT_TYPICAL) {
+        row_stats_kernel<true><<<g1, kStatThreads, 0, st>>>(logits, V, nchunk, inv_t, stats);
+    } else {
+        row_stats_kernel<false><<<g1, kStatThreads, 0, st>>>(logits, V, nchunk, inv_t, stats);
+    }
+    int rc = check_launch("row_stats");
+    if (rc) return rc;
+    if (mode == MEDUSA_ACCEPT_TYPICAL)
+        accept_tree_kernel<true><<<B, kAcceptThreads, 0, st>>>(
+            logits, cand, parent, depth, N, V, Dmax, nchunk, inv_t, eps, delta, stats, accept_len,
+            best_node, path_nodes, next_tok);
+    else
+        accept_tree_kernel<false><<<B, kAcceptThreads, 0, st>>>(
+            logits, cand, parent, depth, N, V, Dmax, nchunk, inv_t, eps, delta, stats, accept_len,
+            best_node, path_nodes, next_tok);
+    return check_launch("accept_tree");
+}
+
+extern "C" size_t medusa_verify_chain_workspace(int B, int gamma, int V) {
+    if (B < 1 || gamma < 0 || V < 1) return 0;
+    return plan_chain(B, V).ws_bytes;
+}
+
+extern "C" int medusa_verify_accept_chain(const float* p, const float* q, const int32_t* draft,
+                                          int B, int gamma, int V, uint64_t seed, uint64_t round,
+                                          int32_t* n_acc, int32_t* out_tok, void* ws,
+                                          size_t ws_bytes, void* stream) {
+    if (!p || (gamma > 0 && (!q || !draft)) || !n_acc || !out_tok)
+        return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_chain: null pointer");
+    if (B < 1 || gamma < 0 || V < 1 || B > 65535)
+        return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_chain: bad sizes");
+    ChainPlan plan = plan_chain(B, V);
+    if (!ws || ws_bytes < plan.ws_bytes)
+        return fail(MEDUSA_ERR_WORKSPACE, "verify_accept_chain: workspace of %zu bytes needed, %zu given",
+                    plan.ws_bytes, ws ? ws_bytes : (size_t)0);
+    if (!aligned16(ws)) return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_chain: ws must be 16-byte aligned");
+    ChainPart* parts = reinterpret_cast<ChainPart*>(static_cast<char*>(ws) + plan.off_parts);
+    int* firsts = reinterpret_cast<int*>(static_cast<char*>(ws) + plan.off_first);
+    cudaStream_t st = as_stream(stream);
+    chain_scan_kernel<<<dim3(plan.nchunk, B), kChainThreads, 0, st>>>(p, q, draft, gamma, V,
+                                                                      plan.nchunk, seed, round,
+                                                                      parts, firsts);
+    int rc = check_launch("chain_scan");
+    if (rc) return rc;
+    chain_finish_kernel<<<B, 32, 0, st>>>(parts, firsts, draft, gamma, plan.nchunk, n_acc, out_tok);
+    return check_launch("chain_finish");
+}

@@ -23,3 +23,15 @@ def read_golden(name):
 @pytest.fixture(scope="session")
 def golden():
     return read_golden
+
+
+@pytest.fixture(scope="session")
+def medusa():
+    """The CUDA library's binding, built in-tree if needed (GPU tests only)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test ran without a CUDA device")
+    from medusa_speculative_decoding_gb300 import build
+    build.build()
+    import medusa_speculative_decoding_gb300 as M
+    return M

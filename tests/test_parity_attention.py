@@ -1,0 +1,88 @@
+"""GPU parity of medusa_tree_attention against the oracle (Medusa Heads glossary
+page, "Tree attention and acceptance")."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import oracle as O
+from util import to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+def _tree(kind):
+    if kind == "c1":
+        return O.tree_layout(O.product_tree_paths((2, 3)), 2)
+    if kind == "sparse64":
+        return O.tree_layout(O.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5)
+    if kind == "dense":
+        return O.tree_layout(O.product_tree_paths((4, 4, 4, 4)), 4)
+    if kind == "small":
+        return O.tree_layout(O.sparse_tree_paths(20, 4, 4, 0.6, 0.5), 4)
+    raise KeyError(kind)
+
+
+def _run(M, x, kv_len, t, scale):
+    out = M.tree_attention(to_dev(x["q"]), to_dev(x["k_cache"]), to_dev(x["v_cache"]),
+                           to_dev(kv_len), to_dev(t["mask"]), scale=scale)
+    torch.cuda.synchronize()
+    return to_np(out)
+
+
+@pytest.mark.parametrize("kind,B,Hq,Hkv,D,lens,Lmax,dtype", [
+    ("c1", 1, 4, 4, 64, [128], 137, "f32"),
+    ("small", 2, 3, 3, 128, [0, 33], 80, "f32"),
+    ("sparse64", 3, 4, 4, 128, [0, 70, 500], 600, "bf16"),
+    ("small", 2, 8, 2, 64, [5, 190], 240, "bf16"),
+    ("dense", 1, 2, 2, 128, [300], 700, "bf16"),
+    ("c1", 4, 4, 4, 64, [1, 63, 64, 65], 80, "bf16"),
+])
+def test_attention_full_compare(medusa, kind, B, Hq, Hkv, D, lens, Lmax, dtype):
+    t = _tree(kind)
+    x = W.attention_inputs(seed=B + Hq + D, B=B, N=t["N"], Hq=Hq, Hkv=Hkv, D=D, Lmax=Lmax, dtype=dtype)
+    kv_len = np.array(lens, np.int32)
+    scale = float(np.float32(1 / np.sqrt(D)))
+    got = _run(medusa, x, kv_len, t, scale)
+    ref = O.tree_attention(x["q"], x["k_cache"], x["v_cache"], kv_len, t["mask"], dtype, scale)
+    assert np.abs(got - ref).max() <= TOL
+
+
+def _sample_rows(B, N, Hq, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.stack([rng.integers(0, B, n), rng.integers(0, N, n), rng.integers(0, Hq, n)], 1)
+    rows[0] = [0, 0, 0]
+    rows[1] = [B - 1, N - 1, Hq - 1]
+    return rows.astype(np.int32)
+
+
+@pytest.mark.parametrize("cfg,kind", [(2, "sparse64"), (3, "sparse64"), (4, "dense"), (4, "sparse64")])
+def test_attention_full_size_sampled(medusa, cfg, kind):
+    c = W.CONFIGS[cfg]
+    t = _tree(kind)
+    N = t["N"]
+    kv_len = W.kv_lengths(cfg, c["B"], c["L_lo"], c["L_hi"])
+    Lmax = c["L_hi"] + N
+    x = W.attention_inputs(seed=cfg, B=c["B"], N=N, Hq=c["Hq"], Hkv=c["Hkv"], D=c["D"], Lmax=Lmax,
+                           dtype=c["dtype"])
+    scale = float(np.float32(1 / np.sqrt(c["D"])))
+    got = _run(medusa, x, kv_len, t, scale)
+    rows = _sample_rows(c["B"], N, c["Hq"], 96, seed=cfg)
+    ref = O.tree_attention(x["q"], x["k_cache"], x["v_cache"], kv_len, t["mask"], c["dtype"], scale,
+                           rows=rows)
+    sel = got[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert np.abs(sel - ref).max() <= TOL
+    assert np.isfinite(got).all()
+
+
+def test_out_of_range_kv_len_is_clamped(medusa):
+    # kv_len beyond Lmax - N is clamped to Lmax - N (no read past the cache)
+    t = _tree("c1")
+    x = W.attention_inputs(seed=5, B=2, N=t["N"], Hq=2, Hkv=2, D=64, Lmax=100, dtype="bf16")
+    scale = 0.125
+    got = _run(medusa, x, np.array([10**6, -5], np.int32), t, scale)
+    ref = O.tree_attention(x["q"], x["k_cache"], x["v_cache"], np.array([100 - t["N"], 0], np.int32),
+                           t["mask"], "bf16", scale)
+    assert np.abs(got - ref).max() <= TOL

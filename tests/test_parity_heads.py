@@ -1,0 +1,73 @@
+"""GPU parity of medusa_heads_topk against the oracle (Medusa Heads glossary
+page, "How heads predict later tokens")."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import oracle as O
+from util import to_dev, to_np, topk_near_tie_ok
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(M, x, topk):
+    idx, val, lg = M.heads_topk(to_dev(x["h"]), to_dev(x["w1"]), to_dev(x["b1"]), to_dev(x["w2"]),
+                                topk, want_logits=True)
+    torch.cuda.synchronize()
+    return to_np(idx), to_np(val), to_np(lg)
+
+
+@pytest.mark.parametrize("B,H,V,K,topk,dtype,tol", [
+    (1, 256, 1000, 3, 3, "f32", 1e-5),      # tiny fp32 step
+    (1, 512, 3001, 5, 8, "bf16", 2e-2),     # several slices, ragged vocab tail
+    (3, 512, 3001, 5, 8, "bf16", 2e-2),
+    (8, 1024, 2000, 2, 16, "bf16", 2e-2),
+    (5, 264, 777, 4, 5, "f32", 1e-5),
+])
+def test_heads_small(medusa, B, H, V, K, topk, dtype, tol):
+    x = W.heads_inputs(seed=B * 7 + K, B=B, H=H, V=V, K=K, dtype=dtype, b1_std=0.5)
+    idx, val, lg = _run(medusa, x, topk)
+    ref = O.heads_logits(x["h"], x["w1"], x["b1"], x["w2"], dtype)
+    assert np.abs(lg - ref).max() <= tol
+    ridx, rval = O.topk(ref, topk)
+    topk_near_tie_ok(idx, ridx, ref)
+    assert np.abs(val - rval).max() <= tol
+
+
+def test_zero_init_heads_reproduce_lm_head(medusa):
+    # hidden 256, vocab 1000, 3 heads, W1 = b1 = 0 and W2_k = lm_head: every head's
+    # logits are bitwise equal on the GPU and match lm_head h from the oracle
+    x = W.heads_inputs(seed=1, B=1, H=256, V=1000, K=3, dtype="f32", zero_init=True)
+    idx, val, lg = _run(medusa, x, 3)
+    assert [bool(np.array_equal(lg[:, k], lg[:, 0])) for k in range(3)] == [True, True, True]
+    lm = O.lm_head_logits(x["h"], x["lm_head"], "f32")
+    assert np.abs(lg[:, 0] - lm).max() <= 1e-5
+    ridx, _ = O.topk(lm, 3)
+    for k in range(3):
+        topk_near_tie_ok(idx[:, k], ridx, lm)
+
+
+@pytest.mark.parametrize("cfg,sample", [(2, None), (3, [0, 5]), (4, [2])])
+def test_heads_full_size(medusa, cfg, sample):
+    c = W.CONFIGS[cfg]
+    x = W.heads_inputs(seed=cfg, B=c["B"], H=c["H"], V=c["V"], K=c["K"], dtype=c["dtype"])
+    idx, val, lg = _run(medusa, x, c["topk"])
+    rows = list(range(c["B"])) if sample is None else sample
+    ref = O.heads_logits(x["h"][rows], x["w1"], x["b1"], x["w2"], c["dtype"])
+    assert np.abs(lg[rows] - ref).max() <= 2e-2
+    ridx, _ = O.topk(ref, c["topk"])
+    topk_near_tie_ok(idx[rows], ridx, ref)
+
+
+def test_workspace_and_alignment_errors(medusa):
+    x = W.heads_inputs(seed=3, B=1, H=256, V=1000, K=3, dtype="f32")
+    args = [to_dev(x[n]) for n in ("h", "w1", "b1", "w2")]
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(medusa.MedusaError) as e:
+        medusa.heads_topk(*args, 3, ws=small)
+    assert e.value.code == -3
+    w2 = torch.empty(args[3].numel() + 1, dtype=torch.float32, device="cuda")[1:].view_as(args[3])
+    with pytest.raises(medusa.MedusaError) as e:
+        medusa.heads_topk(args[0], args[1], args[2], w2, 3)
+    assert e.value.code == -1

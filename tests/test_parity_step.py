@@ -1,0 +1,66 @@
+"""One whole Medusa decode step on the GPU (heads -> tree -> tree attention ->
+acceptance -> KV compaction) against the same step in the oracle, on the tiny
+fp32 workload and on the Vicuna-7B-shaped batch-1 workload."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import oracle as O
+from util import to_dev, to_np, topk_near_tie_ok
+
+pytestmark = pytest.mark.gpu
+
+
+def _tree(c):
+    if c["tree"] == "product":
+        paths = O.product_tree_paths(c["tree_ranks"])
+        return O.tree_layout(paths, len(c["tree_ranks"]))
+    return O.tree_layout(O.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5)
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_full_step(medusa, cfg):
+    M = medusa
+    c = W.CONFIGS[cfg]
+    t = _tree(c)
+    N, Dmax = t["N"], t["max_depth"]
+    dt = c["dtype"]
+    heads = W.heads_inputs(cfg, c["B"], c["H"], c["V"], c["K"], dt)
+    kv_len = W.kv_lengths(cfg, c["B"], c["L_lo"], c["L_hi"])
+    Lmax = c["L_hi"] + N
+    att = W.attention_inputs(cfg, c["B"], N, c["Hq"], c["Hkv"], c["D"], Lmax, dt)
+    ht = W.hidden_tree(cfg, c["B"], N, c["H"], dt)
+    root = W.root_tokens(cfg, c["B"], c["V"])
+    scale = float(np.float32(1 / np.sqrt(c["D"])))
+
+    # oracle step
+    ref_logits = O.heads_logits(heads["h"], heads["w1"], heads["b1"], heads["w2"], dt)
+    ref_idx, _ = O.topk(ref_logits, c["topk"])
+    ref_cand = O.build_tree(ref_idx, root, t["depth"], t["rank"])
+    ref_att = O.tree_attention(att["q"], att["k_cache"], att["v_cache"], kv_len, t["mask"], dt, scale)
+    vlogits = W.planted_logits(cfg, ref_cand, t["parent"], c["V"], c["alpha"])
+    ref_acc = O.verify_tree(vlogits, ref_cand, t["parent"], t["depth"], Dmax)
+    ref_k, ref_v, ref_kl, ref_hn, ref_src = O.kv_compact(
+        att["k_cache"], att["v_cache"], kv_len, ref_acc["path_nodes"], ref_acc["accept_len"],
+        ref_acc["best_node"], ht, N, Dmax)
+
+    # GPU step, all through the C ABI
+    dev = {k: to_dev(v) for k, v in heads.items()}
+    idx, val, _ = M.heads_topk(dev["h"], dev["w1"], dev["b1"], dev["w2"], c["topk"])
+    cand = M.build_tree(idx, to_dev(root), to_dev(t["depth"]), to_dev(t["rank"]))
+    kc, vc, kl = to_dev(att["k_cache"]), to_dev(att["v_cache"]), to_dev(kv_len)
+    o = M.tree_attention(to_dev(att["q"]), kc, vc, kl, to_dev(t["mask"]), scale=scale)
+    acc = M.verify_accept_tree(to_dev(vlogits), cand, to_dev(t["parent"]), to_dev(t["depth"]), Dmax)
+    h_next, src = M.kv_compact(kc, vc, kl, acc["path_nodes"], acc["accept_len"], acc["best_node"], N,
+                               Dmax, hidden_tree=to_dev(ht))
+    torch.cuda.synchronize()
+
+    assert topk_near_tie_ok(to_np(idx), ref_idx, ref_logits) == 0
+    assert np.array_equal(to_np(cand), ref_cand)
+    assert np.abs(to_np(o) - ref_att).max() <= 1e-2
+    for k in ("accept_len", "best_node", "path_nodes", "next_tok"):
+        assert np.array_equal(to_np(acc[k]), ref_acc[k]), k
+    assert np.array_equal(to_np(kc), ref_k) and np.array_equal(to_np(vc), ref_v)
+    assert np.array_equal(to_np(kl), ref_kl)
+    assert np.array_equal(to_np(h_next), ref_hn) and np.array_equal(to_np(src), ref_src)

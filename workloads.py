@@ -93,7 +93,7 @@ def normal(seed: int, stream: str, shape, std: float = 1.0, dtype: str = "f32",
 # heads
 # ----------------------------------------------------------------------------
 def heads_inputs(seed: int, B: int, H: int, V: int, K: int, dtype: str,
-                 w_std: float = 0.02, zero_init: bool = False) -> dict:
+                 w_std: float = 0.02, zero_init: bool = False, b1_std: float = 0.0) -> dict:
     """h [B,H], W1 [K,H,H] (row = output), b1 [K,H], W2 [K,V,H], lm_head [V,H].
 
     With ``zero_init`` W1 = b1 = 0 and every W2_k is a copy of lm_head, the
@@ -108,7 +108,10 @@ def heads_inputs(seed: int, B: int, H: int, V: int, K: int, dtype: str,
         w2 = np.ascontiguousarray(np.broadcast_to(lm, (K, V, H)))
     else:
         w1 = normal(seed, "W1", (K, H, H), w_std, dtype)
-        b1 = np.zeros((K, H), dtype=np.float32 if dtype == "f32" else np.uint16)
+        if b1_std > 0:
+            b1 = normal(seed, "B1", (K, H), b1_std, dtype)
+        else:
+            b1 = np.zeros((K, H), dtype=np.float32 if dtype == "f32" else np.uint16)
         w2 = normal(seed, "W2", (K, V, H), w_std, dtype)
     return dict(h=h, w1=w1, b1=b1, w2=w2, lm_head=lm)
 
