@@ -85,6 +85,28 @@ int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void*
                       int32_t* topk_idx, float* topk_val, float* logits,
                       void* ws, size_t ws_bytes, void* stream);
 
+/* Allocation-free variant of medusa_heads_topk (the pages have no counterpart:
+ * this is a deployment convenience of this library).  Same arguments, results
+ * and limits, minus ws/ws_bytes: the scratch comes from one device array of
+ * MEDUSA_HEADS_STATIC_SCRATCH_BYTES (4 MiB) inside the library, for callers
+ * that cannot call cudaMalloc -- e.g. an operator plugged into a host engine
+ * that owns all device memory and gives its operators no workspace, or a
+ * process whose device memory is fully reserved by a pool it may not grow.
+ *   - Every GPU that loads the library holds that array until process exit.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture on the device.
+ *   - Shapes whose scratch exceeds the maximum (e.g. large B*K*H) return
+ *     MEDUSA_ERR_UNSUPPORTED without launching anything.
+ *   - All calls share the one array: calls whose GPU work overlaps (other
+ *     streams, other host threads on the same device) race and corrupt each
+ *     other's results.  Serialize them, e.g. on one stream.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. */
+#define MEDUSA_HEADS_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
+int medusa_heads_topk_static(const void* h, const void* w1, const void* b1, const void* w2,
+                             medusa_dtype dtype, int B, int K, int H, int V, int topk,
+                             int32_t* topk_idx, float* topk_val, float* logits, void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* 2. Candidate tree  [MH, "Tree attention and acceptance"]                   */
 /*                                                                           */

@@ -4,6 +4,7 @@ The computation lives in libmedusa_gb300.so (hand-written CUDA kernels behind
 the C ABI of include/medusa.h); this package is its thin Python binding:
 
   heads_topk          Medusa heads h + SiLU(W1 h + b1) -> W2, per-head top-k
+  heads_topk_static   the same without a workspace (library-owned scratch)
   sparse_tree_paths   the most accurate rank tuples (host)
   tree_layout         node table, ancestor mask and paths of a tree (host)
   build_tree          candidate tokens of the tree nodes
@@ -13,7 +14,8 @@ the C ABI of include/medusa.h); this package is its thin Python binding:
   kv_compact          keep the accepted branch's KV rows and hidden state
 """
 from ._native import MedusaError, lib  # noqa: F401
-from .api import (build_tree, heads_topk, heads_topk_workspace, kv_compact,  # noqa: F401
+from .api import (build_tree, heads_topk, heads_topk_static, heads_topk_workspace,  # noqa: F401
+                  kv_compact,
                   sparse_tree_paths, tree_attention, tree_attention_workspace, tree_layout,
                   verify_accept_chain, verify_accept_tree, verify_accept_workspace,
                   verify_chain_workspace)

@@ -17,7 +17,7 @@ GREEDY, TYPICAL = 0, 1
 # every symbol include/medusa.h declares
 EXPORTS = (
     "medusa_last_error", "medusa_abi_version",
-    "medusa_heads_topk_workspace", "medusa_heads_topk",
+    "medusa_heads_topk_workspace", "medusa_heads_topk", "medusa_heads_topk_static",
     "medusa_sparse_tree_paths", "medusa_tree_layout", "medusa_build_tree",
     "medusa_tree_attention_workspace", "medusa_tree_attention",
     "medusa_verify_accept_workspace", "medusa_verify_accept_tree",
@@ -48,6 +48,7 @@ def lib() -> C.CDLL:
     L.medusa_heads_topk_workspace.argtypes = [i32] * 5
     L.medusa_heads_topk_workspace.restype = sz
     L.medusa_heads_topk.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P, P, sz, P]
+    L.medusa_heads_topk_static.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P, P]
     L.medusa_sparse_tree_paths.argtypes = [i32, i32, i32, f64, f64, P]
     L.medusa_tree_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P, P]
     L.medusa_build_tree.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P]

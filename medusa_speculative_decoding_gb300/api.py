@@ -76,6 +76,30 @@ def heads_topk(h, w1, b1, w2, topk, want_logits=False, out=None, ws=None, stream
     return idx, val, lg
 
 
+HEADS_STATIC_SCRATCH_BYTES = 4 << 20
+
+
+def heads_topk_static(h, w1, b1, w2, topk, want_logits=False, out=None, stream=None):
+    """heads_topk without a workspace, for callers that cannot allocate device
+    memory: the library's own 4 MiB device scratch array is used instead.  Calls
+    share that array, so calls whose GPU work overlaps race; keep them on one
+    stream."""
+    for n, t in (("h", h), ("w1", w1), ("b1", b1), ("w2", w2)):
+        _need(t, n, h.dtype)
+    B, H = h.shape
+    K, V = w2.shape[0], w2.shape[1]
+    dev = h.device
+    if out is None:
+        idx = torch.empty((B, K, topk), dtype=torch.int32, device=dev)
+        val = torch.empty((B, K, topk), dtype=torch.float32, device=dev)
+        lg = torch.empty((B, K, V), dtype=torch.float32, device=dev) if want_logits else None
+    else:
+        idx, val, lg = out
+    check(lib().medusa_heads_topk_static(_ptr(h), _ptr(w1), _ptr(b1), _ptr(w2), _dtype_of(h), B, K, H,
+                                         V, topk, _ptr(idx), _ptr(val), _ptr(lg), _stream(stream)))
+    return idx, val, lg
+
+
 # ----------------------------------------------------------------------------
 def sparse_tree_paths(n_nodes, max_depth, max_rank, head_p, rank_p):
     out = np.zeros((n_nodes - 1, max_depth), np.int32)

@@ -15,6 +15,8 @@
 #include <float.h>
 #include <limits.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace medusa {
@@ -373,4 +375,69 @@ extern "C" int medusa_heads_topk(const void* h, const void* w1, const void* b1, 
                                         w, p, st);
     return dispatch_batch<float>(B, h, w1, b1, w2, K, H, V, topk, topk_idx, topk_val, logits, w, p,
                                  st);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of medusa_heads_topk.
+//
+// Some callers cannot call cudaMalloc: a plugin or custom operator inside a
+// host inference engine that owns all device memory and hands its operators no
+// workspace, or a process whose device memory is entirely reserved by a pool
+// it may not grow.  For them medusa_heads_topk_static takes its scratch (the
+// float32 z vectors and the per-slice top-k candidates) from one file-scope
+// device array of MEDUSA_HEADS_STATIC_SCRATCH_BYTES instead of a caller buffer.
+// Every GPU that loads this library reserves that array until the process
+// exits.  Host code never passes the array's name to a kernel (in host code it
+// is only a stand-in symbol): the device address comes from
+// cudaGetSymbolAddress, looked up once per device on the first call made with
+// that device current.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_heads_static_scratch[MEDUSA_HEADS_STATIC_SCRATCH_BYTES];
+
+namespace medusa {
+namespace {
+std::mutex g_static_mu;
+void* g_static_ptr[64];
+
+int static_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(MEDUSA_ERR_CUDA, "heads_topk_static: cudaGetDevice failed: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "heads_topk_static: device index %d above 63", dev);
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_heads_static_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(MEDUSA_ERR_CUDA, "heads_topk_static: cudaGetSymbolAddress failed: %s",
+                        cudaGetErrorString(e));
+        g_static_ptr[dev] = p;
+    }
+    *out = g_static_ptr[dev];
+    return MEDUSA_OK;
+}
+}  // namespace
+}  // namespace medusa
+
+extern "C" int medusa_heads_topk_static(const void* h, const void* w1, const void* b1,
+                                        const void* w2, medusa_dtype dtype, int B, int K, int H,
+                                        int V, int topk, int32_t* topk_idx, float* topk_val,
+                                        float* logits, void* stream) {
+    int rc = check_heads_shapes(B, K, H, V, topk);
+    if (rc) return rc;
+    const size_t need = plan_heads(B, K, H, V, topk).ws_bytes;
+    if (need > (size_t)MEDUSA_HEADS_STATIC_SCRATCH_BYTES)
+        return fail(MEDUSA_ERR_UNSUPPORTED,
+                    "heads_topk_static: these shapes need %zu bytes of scratch, above the static "
+                    "maximum of %zu bytes; use medusa_heads_topk with a caller workspace",
+                    need, (size_t)MEDUSA_HEADS_STATIC_SCRATCH_BYTES);
+    void* ws = nullptr;
+    rc = static_scratch(&ws);
+    if (rc) return rc;
+    // No scratch byte needs to start at zero: the call writes every byte it
+    // reads (z before the vocab pass, the slice lists before the merge).
+    return medusa_heads_topk(h, w1, b1, w2, dtype, B, K, H, V, topk, topk_idx, topk_val, logits, ws,
+                             (size_t)MEDUSA_HEADS_STATIC_SCRATCH_BYTES, stream);
 }
