@@ -197,32 +197,35 @@ class Step:
         self.M.build_tree(self.idx, self.root, self.depth, self.rank, out=self.cand)
         cand = self.cand.cpu().numpy()
         self.vlogits = td(W.planted_logits(2, cand, t["parent"], V, c["alpha"]))
-        self.launches = 3 + 1 + (2 if self.ws_att_n > 0 else 1) + 2 + 2
+        # heads 2 (W1, W2 with the merge) + tree 1 + attention 1-2 + verify 2 + compaction 1
+        self.launches = 2 + 1 + (2 if self.ws_att_n > 0 else 1) + 2 + 1
 
     def heads(self):
         c = CFG
         self.M.heads_topk(self.h, self.w1, self.b1, self.w2, c["topk"], out=(self.idx, self.val, None),
                           ws=self.ws_heads)
 
+    CALLS = ("heads_topk", "build_tree", "tree_attention", "verify_accept_tree", "kv_compact")
+
     def run(self, ev=None):
+        """One step; ev (6 events) brackets the five calls when given."""
         M = self.M
         self.kv_len.copy_(self.kv_len0)
-        if ev is not None:
-            ev[0].record()
+        rec = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
+        rec(0)
         self.heads()
-        if ev is not None:
-            ev[1].record()
+        rec(1)
         M.build_tree(self.idx, self.root, self.depth, self.rank, out=self.cand)
-        if ev is not None:
-            ev[2].record()
+        rec(2)
         M.tree_attention(self.q, self.kc, self.vc, self.kv_len, self.mask, out=self.att_out, ws=self.ws_att)
-        if ev is not None:
-            ev[3].record()
+        rec(3)
         M.verify_accept_tree(self.vlogits, self.cand, self.parent, self.depth, self.Dmax, out=self.acc,
                              ws=self.ws_ver)
+        rec(4)
         M.kv_compact(self.kc, self.vc, self.kv_len, self.acc["path_nodes"], self.acc["accept_len"],
                      self.acc["best_node"], self.N, self.Dmax, hidden_tree=self.ht, h_next=self.h_next,
                      src_idx=self.src)
+        rec(5)
 
 
 def run_e2e(step, steps, warmup):
@@ -388,7 +391,6 @@ def main():
     torch.cuda.synchronize()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
@@ -396,10 +398,17 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    # headline: K steps back to back, events only at the two ends (an event between
+    # two calls would stop the next kernel from being scheduled early)
     start.record(stream)
     for i in range(K):
-        step.run(evs[i])
+        step.run()
     end.record(stream)
+    torch.cuda.synchronize()
+    # per-call durations: the same K steps with an event around every call
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for i in range(K):
+        step.run(evs[i])
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -409,8 +418,10 @@ def main():
         t = torch.tensor([ms_total], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_total = float(t.item())
-    heads_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(K))
-    att_ms = statistics.mean(evs[i][2].elapsed_time(evs[i][3]) for i in range(K))
+    call_ms = {name: statistics.mean(evs[i][c].elapsed_time(evs[i][c + 1]) for i in range(K))
+               for c, name in enumerate(Step.CALLS)}
+    heads_ms = call_ms["heads_topk"]
+    att_ms = call_ms["tree_attention"]
     ms_step = ms_total / K
     value = world * K / (ms_total / 1e3)
 
@@ -437,6 +448,7 @@ def main():
                          "ms": heads_ms},
             "attention": {"achieved": att_gbs, "unit": "GB/s", "frac": att_gbs / peak,
                           "algorithmic_bytes": ab, "ms": att_ms},
+            "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
             "clocks": clocks,
             "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

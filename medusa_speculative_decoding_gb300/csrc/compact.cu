@@ -6,17 +6,16 @@
 // L_b .. L_b + a so the cache holds the accepted text in order.  A row's
 // destination can be the source of a later row of the same head, so each block
 // first reads every row it moves into shared memory and only then writes.
-//   kv_compact_rows_kernel : grid (B, head groups); also gathers h_next and
-//                            writes the source slots for sequence b
-//   kv_len_update_kernel   : kv_len[b] += a + 1 (a separate launch: every block
-//                            of the first kernel reads kv_len[b])
+//   kv_compact_kernel : one block per sequence: moves the rows head chunk by
+//                       head chunk, gathers h_next, writes the source slots and
+//                       advances kv_len[b]
 #include "common.cuh"
 
 namespace medusa {
 namespace {
 
-constexpr int kCompactThreads = 256;
-constexpr int kHeadsPerBlock = 8;
+constexpr int kCompactThreads = 512;
+constexpr size_t kCompactSmem = 64 * 1024;  // staging buffer per block
 
 // true iff sequence b's inputs are in range (otherwise it is left unchanged)
 __device__ __forceinline__ bool seq_ok(const int32_t* kv_len, const int32_t* path_nodes,
@@ -31,56 +30,61 @@ __device__ __forceinline__ bool seq_ok(const int32_t* kv_len, const int32_t* pat
     return true;
 }
 
-__global__ void __launch_bounds__(kCompactThreads) kv_compact_rows_kernel(
-    uint4* __restrict__ kc, uint4* __restrict__ vc, const int32_t* __restrict__ kv_len,
+// One block per sequence.  Heads are moved in chunks that fit the staging
+// buffer: every row of a chunk is read before any is written.  The block then
+// gathers h_next, writes the source slots and finally advances kv_len[b] (no
+// other block reads it).
+__global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(
+    uint4* __restrict__ kc, uint4* __restrict__ vc, int32_t* __restrict__ kv_len,
     const int32_t* __restrict__ path_nodes, const int32_t* __restrict__ accept_len,
     const int32_t* __restrict__ best_node, const uint4* __restrict__ hidden_tree,
     uint4* __restrict__ h_next, int Hkv, int row16, int Lmax, int N, int h16, int Dmax,
     int32_t* __restrict__ src_idx) {
-    extern __shared__ uint4 buf[];  // [2][heads][Dmax+1][row16]
+    extern __shared__ uint4 buf[];
+    __shared__ int s_ok, s_a, s_L;
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
-    const int h0 = blockIdx.y * kHeadsPerBlock;
-    const int nh = min(kHeadsPerBlock, Hkv - h0);
-    const bool ok = seq_ok(kv_len, path_nodes, accept_len, best_node, b, N, Lmax, Dmax);
-    if (blockIdx.y == 0 && src_idx) {
-        for (int i = threadIdx.x; i <= Dmax; i += blockDim.x) {
-            const int a = accept_len[b];
-            src_idx[(size_t)b * (Dmax + 1) + i] =
-                !ok ? -2 : (i <= a ? kv_len[b] + path_nodes[(size_t)b * (Dmax + 1) + i] : -1);
-        }
+    if (threadIdx.x == 0) {
+        s_ok = seq_ok(kv_len, path_nodes, accept_len, best_node, b, N, Lmax, Dmax);
+        s_a = accept_len[b];
+        s_L = kv_len[b];
     }
-    if (!ok) return;
-    const int a = accept_len[b], L = kv_len[b];
+    __syncthreads();
+    const bool ok = s_ok;
+    const int a = s_a, L = s_L;
     const int32_t* path = path_nodes + (size_t)b * (Dmax + 1);
-    if (blockIdx.y == 0 && hidden_tree && h_next) {
+    if (src_idx)
+        for (int i = threadIdx.x; i <= Dmax; i += blockDim.x)
+            src_idx[(size_t)b * (Dmax + 1) + i] = !ok ? -2 : (i <= a ? L + path[i] : -1);
+    if (!ok) return;
+    if (hidden_tree && h_next) {
         const uint4* src = hidden_tree + ((size_t)b * N + best_node[b]) * h16;
         for (int i = threadIdx.x; i < h16; i += blockDim.x) h_next[(size_t)b * h16 + i] = src[i];
     }
-    const int per_cache = nh * (a + 1) * row16;
-    for (int t = threadIdx.x; t < 2 * per_cache; t += blockDim.x) {
-        const int c = t / per_cache, r = t % per_cache;
-        const int h = r / ((a + 1) * row16), i = (r / row16) % (a + 1), e = r % row16;
-        const uint4* cache = c ? vc : kc;
-        const size_t row = ((size_t)b * Hkv + h0 + h) * Lmax + L + path[i];
-        buf[t] = cache[row * row16 + e];
+    const int per_head = (a + 1) * row16;  // uint4 per head per cache
+    const int cap_heads = max(1, (int)(kCompactSmem / sizeof(uint4)) / (2 * per_head));
+    for (int h0 = 0; h0 < Hkv; h0 += cap_heads) {
+        const int nh = min(cap_heads, Hkv - h0);
+        const int per_cache = nh * per_head;
+        for (int t = threadIdx.x; t < 2 * per_cache; t += blockDim.x) {
+            const int c = t / per_cache, r = t % per_cache;
+            const int h = r / per_head, i = (r / row16) % (a + 1), e = r % row16;
+            const uint4* cache = c ? vc : kc;
+            const size_t row = ((size_t)b * Hkv + h0 + h) * Lmax + L + path[i];
+            buf[t] = cache[row * row16 + e];
+        }
+        __syncthreads();
+        for (int t = threadIdx.x; t < 2 * per_cache; t += blockDim.x) {
+            const int c = t / per_cache, r = t % per_cache;
+            const int h = r / per_head, i = (r / row16) % (a + 1), e = r % row16;
+            uint4* cache = c ? vc : kc;
+            const size_t row = ((size_t)b * Hkv + h0 + h) * Lmax + L + i;
+            cache[row * row16 + e] = buf[t];
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    for (int t = threadIdx.x; t < 2 * per_cache; t += blockDim.x) {
-        const int c = t / per_cache, r = t % per_cache;
-        const int h = r / ((a + 1) * row16), i = (r / row16) % (a + 1), e = r % row16;
-        uint4* cache = c ? vc : kc;
-        const size_t row = ((size_t)b * Hkv + h0 + h) * Lmax + L + i;
-        cache[row * row16 + e] = buf[t];
-    }
-}
-
-__global__ void kv_len_update_kernel(int32_t* __restrict__ kv_len, const int32_t* __restrict__ path_nodes,
-                                     const int32_t* __restrict__ accept_len,
-                                     const int32_t* __restrict__ best_node, int B, int N, int Lmax,
-                                     int Dmax) {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= B) return;
-    if (seq_ok(kv_len, path_nodes, accept_len, best_node, b, N, Lmax, Dmax)) kv_len[b] += accept_len[b] + 1;
+    if (threadIdx.x == 0) kv_len[b] = L + a + 1;
 }
 
 }  // namespace
@@ -107,20 +111,16 @@ extern "C" int medusa_kv_compact(void* k_cache, void* v_cache, int32_t* kv_len,
     if (!aligned16(k_cache) || !aligned16(v_cache) || (hidden_tree && (!aligned16(hidden_tree) || !aligned16(h_next))))
         return fail(MEDUSA_ERR_INVALID_ARG, "kv_compact: caches and hidden states must be 16-byte aligned");
     const int row16 = D * elem / 16;
-    const size_t smem = (size_t)2 * kHeadsPerBlock * (Dmax + 1) * row16 * sizeof(uint4);
-    if (smem > (size_t)max_smem_optin())
-        return fail(MEDUSA_ERR_UNSUPPORTED, "kv_compact: Dmax %d needs %zu bytes of shared memory", Dmax, smem);
+    if ((size_t)2 * (Dmax + 1) * row16 * sizeof(uint4) > kCompactSmem)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "kv_compact: Dmax %d with D %d does not fit the staging buffer",
+                    Dmax, D);
     cudaStream_t st = as_stream(stream);
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(kv_compact_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    dim3 grid(B, (Hkv + kHeadsPerBlock - 1) / kHeadsPerBlock);
-    kv_compact_rows_kernel<<<grid, kCompactThreads, smem, st>>>(
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), kv_len, path_nodes, accept_len,
-        best_node, static_cast<const uint4*>(hidden_tree), static_cast<uint4*>(h_next), Hkv, row16,
-        Lmax, N, hidden_tree ? H * elem / 16 : 0, Dmax, src_idx);
-    int rc = check_launch("kv_compact_rows");
-    if (rc) return rc;
-    kv_len_update_kernel<<<(B + 255) / 256, 256, 0, st>>>(kv_len, path_nodes, accept_len, best_node, B, N,
-                                                            Lmax, Dmax);
-    return check_launch("kv_len_update");
+    cudaFuncSetAttribute(kv_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCompactSmem);
+    cudaError_t e = launch(kv_compact_kernel, dim3(B), dim3(kCompactThreads), kCompactSmem, st,
+                           static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), kv_len,
+                           path_nodes, accept_len, best_node, static_cast<const uint4*>(hidden_tree),
+                           static_cast<uint4*>(h_next), Hkv, row16, Lmax, N,
+                           hidden_tree ? H * elem / 16 : 0, Dmax, src_idx);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "kv_compact: launch failed: %s", cudaGetErrorString(e));
+    return MEDUSA_OK;
 }

@@ -5,13 +5,17 @@
 //
 // At decode batch sizes (B <= 8) both products are matrix-vector products over
 // weights that are read once per step, so the heads are bound by HBM bandwidth:
-//   K1 heads_w1_silu : z[b,k,:] = h[b] + SiLU(W1_k h[b] + b1_k)   (float32 z)
+//   K1 heads_w1_silu : z[b,k,:] = h[b] + SiLU(W1_k h[b] + b1_k)   (float32 z);
+//                      the K*H rows of W1 are split evenly over the warps of
+//                      one wave of CTAs
 //   K2 heads_w2_topk : logits = W2_k z, streamed over vocab slices; each CTA keeps
-//                      its slice's logits in shared memory and emits its top-k
-//   K3 topk_merge    : merges the per-slice lists into the final sorted top-k
-// Each warp walks R weight rows at once with 16-byte loads (lanes stride over
-// the hidden dimension); the vectors z / h live in shared memory as float32 and
-// are read once per R rows.
+//                      its slice's logits in shared memory and emits its top-k;
+//                      the last CTA of a head merges the head's slice lists
+//                      into the final sorted top-k
+// Each warp walks a few weight rows at once with 16-byte loads (lanes stride
+// over the hidden dimension); the vectors z / h live in shared memory as float32
+// and are read once per group of rows.  K2 is launched as a programmatic
+// dependent of K1 and prefetches its first W2 rows into L2 before it waits for z.
 #include <float.h>
 #include <limits.h>
 
@@ -22,8 +26,11 @@
 namespace medusa {
 namespace {
 
-constexpr int kRows = 4;    // weight rows a warp reduces together
-constexpr int kUnroll = 2;  // 16-byte chunks per row in flight per lane
+constexpr int kRows2 = 4;    // W2 rows a warp reduces together
+constexpr int kUnroll2 = 2;  // 16-byte chunks per W2 row in flight per lane
+constexpr int kRows1 = 2;    // W1 rows a warp reduces together (finer, for balance)
+constexpr int kUnroll1 = 4;
+constexpr int kPrefetchRows = 8;  // W2 rows per CTA prefetched into L2 before the wait
 
 template <typename WT>
 struct Elems { static constexpr int n = 16 / sizeof(WT); };
@@ -64,41 +71,41 @@ __device__ __forceinline__ float dot_chunk<float>(const uint4& w, const float* x
     return acc;
 }
 
-// Partial dot products of rows row0..row0+kRows-1 of W ([rows][H]) with the NB
+// Partial dot products of rows row0..row0+R-1 of W ([rows][H]) with the NB
 // shared-memory vectors xs[b*H ..].  Rows past last_row repeat last_row (their
 // results are discarded by the caller).  Each lane covers chunks lane, lane+32..
-template <typename WT, int NB>
+template <typename WT, int NB, int R, int U>
 __device__ __forceinline__ void dot_rows(const WT* __restrict__ W, int row0, int last_row, int H,
-                                         const float* __restrict__ xs, float (&acc)[kRows][NB],
+                                         const float* __restrict__ xs, float (&acc)[R][NB],
                                          int lane) {
     constexpr int VEC = Elems<WT>::n;
     const int nchunk = H / VEC;
-    const char* rp[kRows];
+    const char* rp[R];
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {
+    for (int r = 0; r < R; ++r) {
         int row = min(row0 + r, last_row);
         rp[r] = reinterpret_cast<const char*>(W + (size_t)row * H);
 #pragma unroll
         for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
     }
-    for (int c0 = lane; c0 < nchunk; c0 += 32 * kUnroll) {
-        uint4 w[kUnroll][kRows];
+    for (int c0 = lane; c0 < nchunk; c0 += 32 * U) {
+        uint4 w[U][R];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int c = c0 + 32 * u;
 #pragma unroll
-            for (int r = 0; r < kRows; ++r)
+            for (int r = 0; r < R; ++r)
                 w[u][r] = c < nchunk ? ld_stream16(rp[r] + (size_t)c * 16) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int c = c0 + 32 * u;
             if (c < nchunk) {
                 const float* xc = xs + (size_t)c * VEC;
 #pragma unroll
                 for (int b = 0; b < NB; ++b)
 #pragma unroll
-                    for (int r = 0; r < kRows; ++r)
+                    for (int r = 0; r < R; ++r)
                         acc[r][b] = dot_chunk<WT>(w[u][r], xc + (size_t)b * H, acc[r][b]);
             }
         }
@@ -110,30 +117,39 @@ __device__ __forceinline__ void load_vector_to_smem(const WT* src, float* dst, i
     for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = load_scalar<WT>(src, i);
 }
 
-// K1: z[b,k,i] = h[b,i] + SiLU(sum_j W1[k,i,j] h[b,j] + b1[k,i])
+// K1: z[b,k,i] = h[b,i] + SiLU(sum_j W1[k,i,j] h[b,j] + b1[k,i]).
+// W1 is walked as K*H consecutive rows (row k*H + i); each warp of the grid
+// takes an equal contiguous range of kRows1-row groups, so one wave of CTAs
+// finishes together.  Block 0 also zeroes the per-head counters that K2 uses to
+// elect the CTA that merges a head's slice lists.
 template <typename WT, int NB, int THREADS>
 __global__ void __launch_bounds__(THREADS) heads_w1_silu_kernel(
     const WT* __restrict__ h, const WT* __restrict__ w1, const WT* __restrict__ b1, int K, int H,
-    int rows_per_cta, float* __restrict__ z) {
+    float* __restrict__ z, unsigned* __restrict__ done) {
     extern __shared__ __align__(16) float xs[];  // [NB][H]
-    const int k = blockIdx.y;
-    const int row_begin = blockIdx.x * rows_per_cta;
-    const int row_end = min(H, row_begin + rows_per_cta);
+    pdl_wait();  // h may come from the previous kernel (the last round's compaction)
+    if (blockIdx.x == 0)
+        for (int k = threadIdx.x; k < K; k += THREADS) done[k] = 0u;
     load_vector_to_smem<WT>(h, xs, NB * H);
     __syncthreads();
-    if (row_begin >= row_end) return;
+    pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const WT* wk = w1 + (size_t)k * H * H;
-    for (int g = row_begin + warp * kRows; g < row_end; g += (THREADS / 32) * kRows) {
-        float acc[kRows][NB];
-        dot_rows<WT, NB>(wk, g, row_end - 1, H, xs, acc, lane);
+    const long long groups = (long long)K * H / kRows1;
+    const long long nwarps = (long long)gridDim.x * (THREADS / 32);
+    const long long gw = (long long)blockIdx.x * (THREADS / 32) + warp;
+    const long long g0 = gw * groups / nwarps, g1 = (gw + 1) * groups / nwarps;
+    for (long long g = g0; g < g1; ++g) {
+        const int row = (int)(g * kRows1);  // kRows1 divides H: a group never spans heads
+        const int k = row / H, i0 = row - k * H;
+        float acc[kRows1][NB];
+        dot_rows<WT, NB, kRows1, kUnroll1>(w1, row, row + kRows1 - 1, H, xs, acc, lane);
 #pragma unroll
-        for (int r = 0; r < kRows; ++r)
+        for (int r = 0; r < kRows1; ++r)
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 const float s = warp_sum(acc[r][b]);
-                const int i = g + r;
-                if (i < row_end && lane == ((r * NB + b) & 31)) {
+                if (lane == ((r * NB + b) & 31)) {
+                    const int i = i0 + r;
                     const float u = s + load_scalar<WT>(b1, (size_t)k * H + i);
                     const float silu = u / (1.f + expf(-u));
                     z[((size_t)b * K + k) * H + i] = xs[(size_t)b * H + i] + silu;
@@ -170,28 +186,42 @@ __device__ __forceinline__ void warp_select_topk(int n, int passes, Get get, Put
 }
 
 // K2: logits of one vocab slice of head k, then the slice's top-k per sequence.
+// The last CTA of head k to finish (elected with an atomic counter that K1
+// zeroed) merges the head's S slice lists into the final sorted top-k.
 template <typename WT, int NB, int THREADS>
 __global__ void __launch_bounds__(THREADS) heads_w2_topk_kernel(
     const WT* __restrict__ w2, const float* __restrict__ z, int K, int H, int V, int rows_per_cta,
-    int topk, float* __restrict__ logits, float* __restrict__ cval, int* __restrict__ cidx) {
+    int topk, float* __restrict__ logits, float* __restrict__ cval, int* __restrict__ cidx,
+    unsigned* __restrict__ done, int32_t* __restrict__ topk_idx, float* __restrict__ topk_val) {
     extern __shared__ __align__(16) float sm[];
     float* xs = sm;                       // [NB][H]
     float* lg = sm + (size_t)NB * H;      // [NB][rows_per_cta]
+    __shared__ bool s_last;
     const int s = blockIdx.x, S = gridDim.x, k = blockIdx.y;
     const int v0 = s * rows_per_cta;
     const int v1 = min(V, v0 + rows_per_cta);
+    const WT* wk = w2 + (size_t)k * V * H;
+    // W2 does not depend on the previous kernel: start pulling this CTA's first
+    // rows into L2 while K1 finishes.
+    if (threadIdx.x == 0) {
+        const int pr = min(kPrefetchRows, v1 - v0);
+        const size_t bytes = (size_t)pr * H * sizeof(WT);
+        if ((bytes & 15) == 0 && bytes > 0)
+            prefetch_l2_bulk(wk + (size_t)v0 * H, (uint32_t)bytes);
+    }
+    pdl_wait();
     for (int i = threadIdx.x; i < NB * H; i += THREADS) {
         const int b = i / H, j = i - b * H;
         xs[i] = z[((size_t)b * K + k) * H + j];
     }
     __syncthreads();
+    pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const WT* wk = w2 + (size_t)k * V * H;
-    for (int g = v0 + warp * kRows; g < v1; g += (THREADS / 32) * kRows) {
-        float acc[kRows][NB];
-        dot_rows<WT, NB>(wk, g, v1 - 1, H, xs, acc, lane);
+    for (int g = v0 + warp * kRows2; g < v1; g += (THREADS / 32) * kRows2) {
+        float acc[kRows2][NB];
+        dot_rows<WT, NB, kRows2, kUnroll2>(wk, g, v1 - 1, H, xs, acc, lane);
 #pragma unroll
-        for (int r = 0; r < kRows; ++r)
+        for (int r = 0; r < kRows2; ++r)
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 const float sum = warp_sum(acc[r][b]);
@@ -212,34 +242,51 @@ __global__ void __launch_bounds__(THREADS) heads_w2_topk_kernel(
             n, topk, [&](int j, float& x, int& xi) { x = row[j]; xi = v0 + j; },
             [&](int t, float v, int i) { ov[t] = v; oi[t] = i; }, lane);
     }
-}
-
-// K3: merge the S per-slice lists of each (b, k) into the sorted top-k.
-__global__ void __launch_bounds__(32) topk_merge_kernel(const float* __restrict__ cval,
-                                                         const int* __restrict__ cidx, int K, int S,
-                                                         int topk, int32_t* __restrict__ topk_idx,
-                                                         float* __restrict__ topk_val) {
-    const int k = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
-    const size_t base = ((size_t)b * K + k) * S * topk;
-    int32_t* oi = topk_idx + ((size_t)b * K + k) * topk;
-    float* ov = topk_val ? topk_val + ((size_t)b * K + k) * topk : nullptr;
-    warp_select_topk(
-        S * topk, topk, [&](int j, float& x, int& xi) { x = cval[base + j]; xi = cidx[base + j]; },
-        [&](int t, float v, int i) {
-            oi[t] = i;
-            if (ov) ov[t] = v;
-        },
-        lane);
+    // Elect the last CTA of head k: make this CTA's lists visible, then count.
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&done[k], 1u) == (unsigned)(S - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // Merge the S lists of each sequence, staged in shared memory when they fit.
+    const int m = S * topk;
+    for (int b = warp; b < NB; b += THREADS / 32) {
+        const size_t base = ((size_t)b * K + k) * S * topk;
+        int32_t* oi = topk_idx + ((size_t)b * K + k) * topk;
+        float* ov = topk_val ? topk_val + ((size_t)b * K + k) * topk : nullptr;
+        // the vectors and slice logits are no longer needed: sequence b stages
+        // its lists in its own (H + rows_per_cta)-float share of shared memory
+        const bool staged = 2 * m <= H + rows_per_cta;
+        float* sv = sm + (size_t)b * (H + rows_per_cta);
+        int* si = reinterpret_cast<int*>(sv + m);
+        if (staged) {
+            for (int j = lane; j < m; j += 32) {
+                sv[j] = __ldcg(cval + base + j);
+                si[j] = __ldcg(cidx + base + j);
+            }
+            __syncwarp();
+        }
+        warp_select_topk(
+            m, topk,
+            [&](int j, float& x, int& xi) {
+                if (staged) { x = sv[j]; xi = si[j]; }
+                else { x = __ldcg(cval + base + j); xi = __ldcg(cidx + base + j); }
+            },
+            [&](int t, float v, int i) {
+                oi[t] = i;
+                if (ov) ov[t] = v;
+            },
+            lane);
+    }
 }
 
 struct HeadsPlan {
     int threads;       // 256 or 512
-    int rows1;         // K1 rows per CTA
-    int grid1;         // K1 CTAs per head
     int rows2;         // K2 vocab rows per CTA
     int S;             // K2 slices per head
     size_t smem1, smem2;
-    size_t off_z, off_val, off_idx, ws_bytes;
+    size_t off_z, off_val, off_idx, off_done, ws_bytes;
 };
 
 HeadsPlan plan_heads(int B, int K, int H, int V, int topk) {
@@ -249,11 +296,6 @@ HeadsPlan plan_heads(int B, int K, int H, int V, int topk) {
     p.threads = big ? 512 : 256;
     const int per_sm = big ? 1 : 2;
     const int target = sm_count() * per_sm;
-    // K1: whole warp-row groups per CTA
-    const int grp = (p.threads / 32) * kRows;
-    int r1 = (int)(((long long)H * K + target - 1) / target);
-    p.rows1 = ((r1 + grp - 1) / grp) * grp;
-    p.grid1 = (H + p.rows1 - 1) / p.rows1;
     // K2: vocab slices so that K * S fills one wave; each slice >= topk rows
     int s0 = target / K;
     if (s0 < 1) s0 = 1;
@@ -273,6 +315,8 @@ HeadsPlan plan_heads(int B, int K, int H, int V, int topk) {
     off = align_up(off + (size_t)B * K * p.S * topk * sizeof(float), 256);
     p.off_idx = off;
     off = align_up(off + (size_t)B * K * p.S * topk * sizeof(int), 256);
+    p.off_done = off;
+    off = align_up(off + (size_t)K * sizeof(unsigned), 256);
     p.ws_bytes = off;
     return p;
 }
@@ -284,23 +328,31 @@ int launch_heads(const void* h, const void* w1, const void* b1, const void* w2, 
     float* z = reinterpret_cast<float*>(ws + p.off_z);
     float* cval = reinterpret_cast<float*>(ws + p.off_val);
     int* cidx = reinterpret_cast<int*>(ws + p.off_idx);
+    unsigned* done = reinterpret_cast<unsigned*>(ws + p.off_done);
     auto k1 = heads_w1_silu_kernel<WT, NB, THREADS>;
     auto k2 = heads_w2_topk_kernel<WT, NB, THREADS>;
     if (p.smem1 > 48 * 1024)
         cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem1);
     if (p.smem2 > 48 * 1024)
         cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem2);
-    k1<<<dim3(p.grid1, K), THREADS, p.smem1, st>>>(static_cast<const WT*>(h),
-                                                   static_cast<const WT*>(w1),
-                                                   static_cast<const WT*>(b1), K, H, p.rows1, z);
-    int rc = check_launch("heads_w1_silu");
-    if (rc) return rc;
-    k2<<<dim3(p.S, K), THREADS, p.smem2, st>>>(static_cast<const WT*>(w2), z, K, H, V, p.rows2,
-                                               topk, logits, cval, cidx);
-    rc = check_launch("heads_w2_topk");
-    if (rc) return rc;
-    topk_merge_kernel<<<dim3(K, NB), 32, 0, st>>>(cval, cidx, K, p.S, topk, topk_idx, topk_val);
-    return check_launch("topk_merge");
+    // K1 grid: exactly the CTAs that fit on the device at once, but no more
+    // warps than row groups.
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k1, THREADS, p.smem1) != cudaSuccess || occ < 1)
+        occ = 1;
+    long long grid1 = (long long)sm_count() * occ;
+    const long long groups = (long long)K * H / kRows1;
+    const long long max_ctas = (groups + THREADS / 32 - 1) / (THREADS / 32);
+    if (grid1 > max_ctas) grid1 = max_ctas;
+    cudaError_t e = launch(k1, dim3((unsigned)grid1), dim3(THREADS), p.smem1, st,
+                           static_cast<const WT*>(h), static_cast<const WT*>(w1),
+                           static_cast<const WT*>(b1), K, H, z, done);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "heads_w1_silu: launch failed: %s", cudaGetErrorString(e));
+    e = launch(k2, dim3(p.S, K), dim3(THREADS), p.smem2, st, static_cast<const WT*>(w2),
+               static_cast<const float*>(z), K, H, V, p.rows2, topk, logits, cval, cidx, done,
+               topk_idx, topk_val);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "heads_w2_topk: launch failed: %s", cudaGetErrorString(e));
+    return MEDUSA_OK;
 }
 
 template <typename WT, int NB>

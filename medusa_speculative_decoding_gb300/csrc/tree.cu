@@ -32,6 +32,8 @@ __global__ void build_tree_kernel(const int32_t* __restrict__ topk_idx,
                                   const int32_t* __restrict__ depth,
                                   const int32_t* __restrict__ rank, int B, int K, int topk, int N,
                                   int32_t* __restrict__ cand) {
+    pdl_wait();
+    pdl_trigger();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= B * N) return;
     const int b = i / N, n = i - b * N;
@@ -172,7 +174,8 @@ extern "C" int medusa_build_tree(const int32_t* topk_idx, const int32_t* root_to
     if (B < 1 || K < 1 || topk < 1 || N < 1)
         return fail(MEDUSA_ERR_INVALID_ARG, "build_tree: sizes must be positive");
     const int total = B * N;
-    build_tree_kernel<<<(total + 255) / 256, 256, 0, as_stream(stream)>>>(topk_idx, root_tok, depth,
-                                                                          rank, B, K, topk, N, cand);
-    return check_launch("build_tree");
+    cudaError_t e = launch(build_tree_kernel, dim3((total + 255) / 256), dim3(256), 0,
+                           as_stream(stream), topk_idx, root_tok, depth, rank, B, K, topk, N, cand);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "build_tree: launch failed: %s", cudaGetErrorString(e));
+    return MEDUSA_OK;
 }

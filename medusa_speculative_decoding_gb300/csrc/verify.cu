@@ -54,6 +54,8 @@ template <bool TYPICAL>
 __global__ void __launch_bounds__(kStatThreads) row_stats_kernel(const float* __restrict__ logits,
                                                                  int V, int nchunk, float inv_t,
                                                                  RowStat* __restrict__ stats) {
+    pdl_wait();
+    pdl_trigger();
     const int c = blockIdx.x, row = blockIdx.y;
     const float* x = logits + (size_t)row * V;
     const int v0 = c * kChunk, v1 = min(V, v0 + kChunk);
@@ -142,6 +144,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_tree_kernel(
     __shared__ float s_m[kAcceptThreads], s_s[kAcceptThreads], s_tau[kAcceptThreads];
     __shared__ unsigned char s_pass[kAcceptThreads];
     __shared__ int s_best;
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const int u = threadIdx.x;
     if (u < N) {
@@ -272,6 +276,8 @@ __global__ void __launch_bounds__(kChainThreads) chain_scan_kernel(
     const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ draft,
     int gamma, int V, int nchunk, uint64_t seed, uint64_t round, ChainPart* __restrict__ parts,
     int* __restrict__ firsts) {
+    pdl_wait();
+    pdl_trigger();
     const int c = blockIdx.x, b = blockIdx.y;
     const int first = first_reject(p, q, draft, gamma, V, b, seed, round);
     if (c == 0 && threadIdx.x == 0) firsts[b] = first;
@@ -322,6 +328,8 @@ __global__ void __launch_bounds__(32) chain_finish_kernel(const ChainPart* __res
                                                           int gamma, int nchunk,
                                                           int32_t* __restrict__ n_acc,
                                                           int32_t* __restrict__ out_tok) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x, lane = threadIdx.x;
     float bk = INFINITY, pm = -INFINITY;
     int bt = INT_MAX, pi = INT_MAX;
@@ -404,22 +412,18 @@ extern "C" int medusa_verify_accept_tree(const float* logits, const int32_t* can
     cudaStream_t st = as_stream(stream);
     const float inv_t = 1.f / temperature;
     dim3 g1(nchunk, B * N);
-    if (mode == MEDUSA_ACCEPT_TYPICAL) {
-        row_stats_kernel<true><<<g1, kStatThreads, 0, st>>>(logits, V, nchunk, inv_t, stats);
-    } else {
-        row_stats_kernel<false><<<g1, kStatThreads, 0, st>>>(logits, V, nchunk, inv_t, stats);
-    }
-    int rc = check_launch("row_stats");
-    if (rc) return rc;
+    cudaError_t e;
     if (mode == MEDUSA_ACCEPT_TYPICAL)
-        accept_tree_kernel<true><<<B, kAcceptThreads, 0, st>>>(
-            logits, cand, parent, depth, N, V, Dmax, nchunk, inv_t, eps, delta, stats, accept_len,
-            best_node, path_nodes, next_tok);
+        e = launch(row_stats_kernel<true>, g1, dim3(kStatThreads), 0, st, logits, V, nchunk, inv_t, stats);
     else
-        accept_tree_kernel<false><<<B, kAcceptThreads, 0, st>>>(
-            logits, cand, parent, depth, N, V, Dmax, nchunk, inv_t, eps, delta, stats, accept_len,
-            best_node, path_nodes, next_tok);
-    return check_launch("accept_tree");
+        e = launch(row_stats_kernel<false>, g1, dim3(kStatThreads), 0, st, logits, V, nchunk, inv_t, stats);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "row_stats: launch failed: %s", cudaGetErrorString(e));
+    auto acc = mode == MEDUSA_ACCEPT_TYPICAL ? accept_tree_kernel<true> : accept_tree_kernel<false>;
+    e = launch(acc, dim3(B), dim3(kAcceptThreads), 0, st, logits, cand, parent, depth, N, V, Dmax,
+               nchunk, inv_t, eps, delta, (const RowStat*)stats, accept_len, best_node, path_nodes,
+               next_tok);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "accept_tree: launch failed: %s", cudaGetErrorString(e));
+    return MEDUSA_OK;
 }
 
 extern "C" size_t medusa_verify_chain_workspace(int B, int gamma, int V) {
@@ -443,11 +447,11 @@ extern "C" int medusa_verify_accept_chain(const float* p, const float* q, const 
     ChainPart* parts = reinterpret_cast<ChainPart*>(static_cast<char*>(ws) + plan.off_parts);
     int* firsts = reinterpret_cast<int*>(static_cast<char*>(ws) + plan.off_first);
     cudaStream_t st = as_stream(stream);
-    chain_scan_kernel<<<dim3(plan.nchunk, B), kChainThreads, 0, st>>>(p, q, draft, gamma, V,
-                                                                      plan.nchunk, seed, round,
-                                                                      parts, firsts);
-    int rc = check_launch("chain_scan");
-    if (rc) return rc;
-    chain_finish_kernel<<<B, 32, 0, st>>>(parts, firsts, draft, gamma, plan.nchunk, n_acc, out_tok);
-    return check_launch("chain_finish");
+cudaError_t e = launch(chain_scan_kernel, dim3(plan.nchunk, B), dim3(kChainThreads), 0, st, p, q,
+                           draft, gamma, V, plan.nchunk, seed, round, parts, firsts);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "chain_scan: launch failed: %s", cudaGetErrorString(e));
+    e = launch(chain_finish_kernel, dim3(B), dim3(32), 0, st, (const ChainPart*)parts,
+               (const int*)firsts, draft, gamma, plan.nchunk, n_acc, out_tok);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "chain_finish: launch failed: %s", cudaGetErrorString(e));
+    return MEDUSA_OK;
 }
