@@ -8,12 +8,11 @@
 // bytes, so the bf16 kernel reads each KV tile once per (sequence, KV head,
 // block of 128 tree queries) and scores all of the block's queries against it
 // on the fifth-generation tensor cores (tcgen05, accumulators in TMEM):
-//   tree_attn_umma_kernel : split-KV over CTAs; per 64-key tile S = Q K^T and
-//                           O += P V as tcgen05.mma (bf16 in, float32 out),
-//                           online softmax in float32 with one query row per
-//                           thread, ancestor bits tested only on tiles that
-//                           reach the tree slots
-//   attn_combine_kernel   : merges the per-split (max, sum, O) partials
+//   tree_attn_umma_kernel : split-KV over a cluster of CTAs; per 64-key tile
+//                           S = Q K^T and O += P V as tcgen05.mma (bf16 in,
+//                           float32 out) fed by TMA; online softmax in float32;
+//                           ancestor bits tested only on tiles that reach the
+//                           tree slots; split partials merged in the cluster
 //   tree_attn_f32_kernel  : float32 storage path (one warp per query row)
 #include <float.h>
 
@@ -52,9 +51,9 @@ struct AttnArgs {
     const int32_t* kv_len;
     const uint64_t* mask;
     float* out;
-    float* part_o;   // [B,Hq,N,S,D]
-    float* part_ml;  // [B,Hq,N,S,2]
     int B, N, Hq, Hkv, G, Lmax, W, S, chunk, qblocks;
+    int q_tma;   // Q tile loaded by TMA
+    int spread;  // query blocks of <= 64 rows spread over the TMEM lane quarters
     float scale_log2;
 };
 
@@ -63,55 +62,84 @@ __device__ __forceinline__ int clamp_len(int L, int N, int Lmax) {
 }
 
 // ---------------------------------------------------------------------------
-// tcgen05 kernel.  One CTA of 256 threads per (KV split, KV head x block of 128
-// tree queries, sequence).  Query row r lives in TMEM lane r; threads r and
-// r + 128 share it, each owning half of every 64-key score tile and half of
-// the output columns.  Per tile j (keys [k_j, k_j + 64)):
-//   S_j = Q K_j^T        tcgen05.mma, float32 in TMEM (two S buffers)
-//   P_j = exp2(S_j * scale * log2e - m)   online softmax in registers, written
-//                        as bf16 to one of two swizzled P buffers
-//   O  += P_j V_j        tcgen05.mma, float32 accumulator in TMEM
-// K and V tiles arrive by TMA (one thread, byte-counted mbarriers) into two
-// 4-deep rings; S_{j+1} is issued before the softmax of tile j, so the tensor
-// core overlaps the softmax.  The last tile of a split is shifted back to end
-// exactly at the split's last key, so no row past it is ever read; keys the
-// shift brings back are masked.  The reference max used for P moves only when
-// the row max grows by more than 2^8 (log2 domain), and O and the row sum are
-// rescaled in TMEM at that moment.
+// tcgen05 kernel.  One CTA per (KV split, KV head x block of 128 tree queries,
+// sequence); the CTAs of one (head, query block) split the keys and form a
+// thread-block cluster.  Query row r lives in TMEM lane r.
+//
+// A block of at most 64 query rows is spread 16 rows per TMEM lane quarter so
+// that all four SM sub-partitions share the softmax.
+//
+// Warp roles (576 threads):
+//   warps 0-15  softmax: thread (r, q), q = tid / 128, owns 16 of the 64
+//               scores of TMEM lane r in every tile and D/4 of its output
+//               columns; the four owners of a row exchange their maxima
+//               through shared memory (one named barrier per tile)
+//   warp 16     MMA: lane 0 issues every tcgen05.mma and commit
+//   warp 17     TMA: lane 0 loads Q and streams K and V tiles into two 4-deep
+//               rings
+// Per 64-key tile j (keys [k_j, k_j + 64)):
+//   S_j = Q K_j^T       tcgen05.mma into TMEM S buffer j & 1      (s_full)
+//   softmax             row max, P_j = exp2(S_j*scale*log2e - m) as bf16 into
+//                       swizzled P buffer j & 1                 (p_full)
+//   O += P_j V_j        tcgen05.mma into the TMEM accumulator    (o_done)
+// The MMA lane issues PV_{j-1} and S_{j+1} while the softmax warps work on tile
+// j.  Every ring stage has a full barrier (TMA bytes landed) and an empty
+// barrier (the MMA that read it completed), so no wait can fall two phases
+// behind.  The last tile of a split is shifted back to end at the split's last
+// key, so no row past it is read; keys the shift brings back are masked.  The
+// reference max moves only when a row max grows by more than 2^8 (log2
+// domain); O and the row sums are rescaled in TMEM then.  Split partials (O,
+// max, sum) are merged across the cluster: after a cluster barrier every CTA
+// stores each row's partial into the shared memory of the CTA that owns the
+// row (rows are dealt round-robin), and after a second barrier each CTA merges
+// its rows from its own shared memory.
+// Every wait is bounded; a CTA that gives up writes NaN.
 // ---------------------------------------------------------------------------
 constexpr int kUmmaM = 128;
-constexpr int kUmmaThreads = 256;
-constexpr int kRingK = 4, kRingV = 4;
+constexpr int kSoftmaxWarps = 16;
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
+constexpr int kAttnThreads = kSoftmaxThreads + 64;
+constexpr int kRing = 4;       // K and V ring depth
+constexpr int kMaxSplits = 8;  // portable cluster size
 constexpr float kRescaleThreshold = 8.f;
 constexpr long long kWaitCycles = 1ll << 31;  // ~1 s at 2 GHz
 
 template <int D>
-struct UmmaSmem {
+struct AttnSmem {
     static constexpr int kQ = kUmmaM * D * 2;
     static constexpr int kTile = kBlockN * D * 2;  // one K or V tile
     static constexpr int kP = kUmmaM * kBlockN * 2;
     static constexpr int kOffK = kQ;
-    static constexpr int kOffV = kOffK + kRingK * kTile;
-    static constexpr int kOffP = kOffV + kRingV * kTile;
-    static constexpr int kOffRed = kOffP + 2 * kP;       // float [2][128]
-    static constexpr int kOffBar = kOffRed + 2 * 128 * 4;  // mbarriers
-    static constexpr int kNumBar = 1 + 2 + kRingK + kRingV;
-    static constexpr int kOffMisc = kOffBar + kNumBar * 8;  // tmem slot, flag
-    static constexpr int kBytes = kOffMisc + 16 + 1024;     // + alignment slack
+    static constexpr int kOffV = kOffK + kRing * kTile;
+    static constexpr int kOffP = kOffV + kRing * kTile;
+    static constexpr int kOffRed = kOffP + 2 * kP;            // float [2][4][128]
+    static constexpr int kOffBar = kOffRed + 2 * 4 * 128 * 4;
+    // kfull[4] vfull[4] kempty[4] vempty[4] s_full[2] o_done[2] p_full[2] qfull
+    static constexpr int kNumBar = 4 * kRing + 7;
+    static constexpr int kOffMisc = kOffBar + kNumBar * 8;    // tmem slot, flag
+    static constexpr int kBytes = kOffMisc + 16 + 1024;       // + alignment slack
+    // after the tile loop the K/V rings receive the partials of the rows this
+    // CTA owns: float O [kMaxSplits][rows_per_owner][D], then (max, sum)
+    static constexpr int kOffPartO = kOffK;
+    static constexpr int kOffPartML = kOffK + (kUmmaM + kMaxSplits) * D * 4;
+    static_assert((kUmmaM + kMaxSplits) * (D + 2) * 4 <= 2 * kRing * kTile, "partials fit the rings");
 };
 
 template <int D>
-__global__ void __launch_bounds__(kUmmaThreads, 1) tree_attn_umma_kernel(
-    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AttnArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
+    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+    const __grid_constant__ CUtensorMap tmq, AttnArgs a) {
     using namespace umma;
-    using L = UmmaSmem<D>;
-    constexpr int CH = D / 8;         // 16-byte chunks per row
-    constexpr int TMEM_COLS = 256;    // O: D columns at 0; S buffers at 128 and 192
+    using L = AttnSmem<D>;
+    constexpr int CH = D / 8;          // 16-byte chunks per row
+    constexpr int TMEM_COLS = 256;     // O: D columns at 0; S buffers at 128 and 192
     constexpr uint32_t kSCol = 128;
-    constexpr int HALF = kBlockN / 2;
+    constexpr int SW = kBlockN / 4;    // scores per softmax thread
+    constexpr int QW = D / 4;          // output columns per softmax thread
     extern __shared__ uint8_t smem_raw[];
 
-    const int split = blockIdx.x;
+    const int split = blockIdx.x, S = gridDim.x;
     const int hk = blockIdx.y / a.qblocks, qb = blockIdx.y % a.qblocks;
     const int b = blockIdx.z;
     const int N = a.N, G = a.G;
@@ -120,13 +148,21 @@ __global__ void __launch_bounds__(kUmmaThreads, 1) tree_attn_umma_kernel(
     const int Lb = clamp_len(a.kv_len[b], N, a.Lmax);
     const int total = Lb + N;
     const int k_begin = split * a.chunk;
-    if (k_begin >= total) return;  // no keys of sequence b in this split (uniform per CTA)
     const int k_end = min(total, k_begin + a.chunk);
-    const int ntiles = (k_end - k_begin + kBlockN - 1) / kBlockN;
+    const int ntiles = k_begin < total ? (k_end - k_begin + kBlockN - 1) / kBlockN : 0;
     const int rows = N * G;
     const int row0 = qb * kUmmaM;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int r = tid & (kUmmaM - 1), half = tid >> 7;
+    const int nblk = min(rows - row0, kUmmaM);  // query rows in this block
+    // A block of at most 64 rows is spread over the four TMEM lane quarters (16
+    // rows each) so all four SM sub-partitions share the softmax; otherwise
+    // block row i is TMEM lane i.
+    const bool spread = a.spread != 0;
+    auto qrow_of = [&](int m) -> int {  // TMEM lane -> block row, -1 for padding
+        const int i = spread ? (((m & 31) < 16) ? 16 * (m >> 5) + (m & 15) : -1) : m;
+        return (i >= 0 && i < nblk) ? i : -1;
+    };
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = tid & (kUmmaM - 1), q = (tid >> 7) & 3;
 
     const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
     uint8_t* base = smem_raw + pad;
@@ -135,321 +171,365 @@ __global__ void __launch_bounds__(kUmmaThreads, 1) tree_attn_umma_kernel(
                    ps_a = base_a + L::kOffP;
     float* red = reinterpret_cast<float*>(base + L::kOffRed);
     const uint32_t bar_a = base_a + L::kOffBar;
-    const uint32_t mbS = bar_a, mbO0 = bar_a + 8;  // mbO[i] = mbO0 + 8 i
-    const uint32_t kfull0 = bar_a + 24, vfull0 = kfull0 + 8 * kRingK;
+    const uint32_t kfull0 = bar_a, vfull0 = kfull0 + 8 * kRing, kempty0 = vfull0 + 8 * kRing,
+                   vempty0 = kempty0 + 8 * kRing, s_full0 = vempty0 + 8 * kRing,
+                   o_done0 = s_full0 + 16, p_full0 = o_done0 + 16, qfull = p_full0 + 16;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kOffMisc);
-    int* flag = reinterpret_cast<int*>(base + L::kOffMisc + 4);
+    volatile int* flag = reinterpret_cast<volatile int*>(base + L::kOffMisc + 4);
 
-    // key range of tile t: [tile_start, tile_start + 64); keys below tile_lo were
-    // covered by an earlier tile (or another split)
     auto tile_lo = [&](int t) { return k_begin + t * kBlockN; };
     auto tile_start = [&](int t) { return min(k_begin + t * kBlockN, k_end - kBlockN); };
     const int zrow = b * a.Hkv + hk;
-    auto load_k = [&](int t) {
-        const uint32_t st = ks_a + (t % kRingK) * L::kTile, fb = kfull0 + 8 * (t % kRingK);
-        mbar_expect_tx(fb, L::kTile);
-#pragma unroll
-        for (int x = 0; x < D / 64; ++x) tma_load_3d(st + x * kBlockN * 128, &tmk, x * 64, tile_start(t), zrow, fb);
-    };
-    auto load_v = [&](int t) {
-        const uint32_t st = vs_a + (t % kRingV) * L::kTile, fb = vfull0 + 8 * (t % kRingV);
-        mbar_expect_tx(fb, L::kTile);
-#pragma unroll
-        for (int x = 0; x < D / 64; ++x) tma_load_3d(st + x * kBlockN * 128, &tmv, x * 64, tile_start(t), zrow, fb);
-    };
 
-    if (tid == 0) {
+    if (warp == kTmaWarp && lane == 0) {
+        // barriers first, then the first K/V tiles, while the softmax warps load Q
         for (int i = 0; i < L::kNumBar; ++i) mbar_init(bar_a + 8 * i, 1);
+        mbar_init(p_full0, kSoftmaxWarps);
+        mbar_init(p_full0 + 8, kSoftmaxWarps);
         mbar_init_fence();
         *flag = 0;
+        if (a.q_tma && ntiles > 0) {  // Q rows (node, group member) x D
+            if (spread) {  // block rows 16g .. 16g+15 -> TMEM lanes 32g .. 32g+15
+                mbar_expect_tx(qfull, 4 * 16 * D * 2);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        tma_load_4d(qs_a + x * kUmmaM * 128 + g * 32 * 128, &tmq, x * 64, hk * G,
+                                    (row0 + 16 * g) / G, b, qfull);
+            } else {
+                mbar_expect_tx(qfull, L::kQ);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+                    tma_load_4d(qs_a + x * kUmmaM * 128, &tmq, x * 64, hk * G, row0 / G, b, qfull);
+            }
+        }
+        for (int t = 0; t < kRing && t < ntiles; ++t) {
+            mbar_expect_tx(kfull0 + 8 * t, L::kTile);
+            mbar_expect_tx(vfull0 + 8 * t, L::kTile);
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x) {
+                tma_load_3d(ks_a + t * L::kTile + x * kBlockN * 128, &tmk, x * 64, tile_start(t), zrow, kfull0 + 8 * t);
+                tma_load_3d(vs_a + t * L::kTile + x * kBlockN * 128, &tmv, x * 64, tile_start(t), zrow, vfull0 + 8 * t);
+            }
+        }
     }
     if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
-    // Q tile: row r -> node r / G, query head hk * G + r % G; padding rows are zero
-    for (int c = tid; c < kUmmaM * CH; c += kUmmaThreads) {
-        const int rr = c / CH, ch = c % CH;
-        const int gr = row0 + rr;
-        const bool ok = gr < rows;
-        const int node = ok ? gr / G : 0, hq = hk * G + (ok ? gr % G : 0);
-        cp_async16(qs_a + sw128_offset(rr, ch, kUmmaM),
-                   a.q + (((size_t)b * N + node) * a.Hq + hq) * D + ch * 8, ok);
+    // Q tile without TMA (group size not dividing 128): row rr -> node rr / G,
+    // query head hk * G + rr % G; padding rows are zero
+    if (!a.q_tma && warp < kSoftmaxWarps) {
+        for (int c = tid; c < kUmmaM * CH; c += kSoftmaxThreads) {
+            const int m = c / CH, ch = c % CH;  // TMEM lane m = MMA row m
+            const int i = qrow_of(m);
+            const bool ok = i >= 0;
+            const int gr = row0 + max(i, 0);
+            const int node = gr / G, hq = hk * G + gr % G;
+            cp_async16(qs_a + sw128_offset(m, ch, kUmmaM),
+                       a.q + (((size_t)b * N + (ok ? node : 0)) * a.Hq + (ok ? hq : 0)) * D + ch * 8, ok);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_async_smem();
     }
-    cp_async_commit();
     fence_before_sync();
-    __syncthreads();  // barriers initialised, TMEM allocated
-    fence_after_sync();
-    int k_issued = 0, v_issued = 0;  // thread 0: K / V tiles requested so far
-    if (tid == 0) {
-        for (; k_issued < kRingK && k_issued < ntiles; ++k_issued) load_k(k_issued);
-        for (; v_issued < kRingV && v_issued < ntiles; ++v_issued) load_v(v_issued);
-    }
-    cp_async_wait<0>();
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();  // Q resident and visible to the tensor core
+    __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-
-    const int grow = row0 + r;
-    const bool valid = grow < rows;
-    const int node = valid ? grow / G : 0;
-    const uint64_t* mrow = a.mask + (size_t)node * a.W;
-    constexpr uint32_t idesc_s = idesc_bf16(kUmmaM, kBlockN, 0, 0);
-    constexpr uint32_t idesc_pv = idesc_bf16(kUmmaM, D, 0, 1);
-
-    // thread 0 only: S_t = Q K_t^T into S buffer t & 1, after K_t has landed
-    auto issue_s = [&](int t) -> bool {
-        if (!mbar_wait(kfull0 + 8 * (t % kRingK), (uint32_t)((t / kRingK) & 1), kWaitCycles)) return false;
-        const uint32_t ka = ks_a + (t % kRingK) * L::kTile;
-        const uint32_t d = tmem + kSCol + (t & 1) * kBlockN;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t ad = desc_sw128(qs_a + (ks >> 2) * (kUmmaM * 128) + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = desc_sw128(ka + (ks >> 2) * (kBlockN * 128) + (ks & 3) * 32, 16, 1024);
-            mma_bf16(d, ad, bd, idesc_s, ks > 0);
-        }
-        commit(mbS);
-        return true;
-    };
-    // thread 0 only: O += P_t V_t, after V_t has landed
-    auto issue_pv = [&](int t) -> bool {
-        if (!mbar_wait(vfull0 + 8 * (t % kRingV), (uint32_t)((t / kRingV) & 1), kWaitCycles)) return false;
-        const uint32_t va = vs_a + (t % kRingV) * L::kTile;
-        const uint32_t pa = ps_a + (t & 1) * L::kP;
-#pragma unroll
-        for (int ks = 0; ks < kBlockN / 16; ++ks) {
-            const uint64_t ad = desc_sw128(pa + ks * 32, 16, 1024);
-            const uint64_t bd = desc_sw128(va + ks * 2048, kBlockN * 128, 1024);
-            mma_bf16(tmem, ad, bd, idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
-        }
-        commit(mbO0 + 8 * (t & 1));
-        return true;
-    };
-    if (tid == 0 && !issue_s(0)) *flag = 1;
 
     float m_ref = -INFINITY, l = 0.f;
     bool bad = false;
-    for (int j = 0; j < ntiles; ++j) {
-        // 1. S_j complete (K_j's stage is free again)
-        bool ok = mbar_wait(mbS, (uint32_t)(j & 1), kWaitCycles);
-        fence_after_sync();
-        // 2. this half-row's 32 scores
-        float sv[HALF];
-        tmem_ld32(tmem + lane_off + kSCol + (j & 1) * kBlockN + half * HALF, sv);
-        tmem_wait_ld();
-        const int kt = tile_start(j), klo = tile_lo(j);
-        const int c0 = kt + half * HALF;  // key of sv[0]
-        float mt = -INFINITY;
-        if (kt == klo && kt + kBlockN <= min(k_end, Lb)) {  // plain prefix tile
+    if (warp == kMmaWarp) {
+        // -------------------------------- MMA lane --------------------------------
+        if (lane == 0 && ntiles > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(kUmmaM, kBlockN, 0, 0);
+            constexpr uint32_t idesc_pv = idesc_bf16(kUmmaM, D, 0, 1);
+            // descriptors of the first k-step; later k-steps add byte offsets >> 4
+            // to the start-address field
+            const uint64_t dq0 = desc_sw128(qs_a, 16, 1024);
+            const uint64_t dk0 = desc_sw128(ks_a, 16, 1024);
+            const uint64_t dp0 = desc_sw128(ps_a, 16, 1024);
+            const uint64_t dv0 = desc_sw128(vs_a, kBlockN * 128, 1024);
+            bool fail = false;
+            auto wait = [&](uint32_t bar, uint32_t parity) {
+                if (fail) return false;
+                if (!mbar_wait(bar, parity, kWaitCycles)) { fail = true; *flag = 1; return false; }
+                return true;
+            };
+            auto issue_s = [&](int t) {  // S_t = Q K_t^T into S buffer t & 1
+                const uint64_t dk = dk0 + (uint64_t)(((t % kRing) * L::kTile) >> 4);
+                const uint32_t d = tmem + kSCol + (t & 1) * kBlockN;
 #pragma unroll
-            for (int i = 0; i < HALF; ++i) { sv[i] *= a.scale_log2; mt = fmaxf(mt, sv[i]); }
-        } else {
-            uint64_t w0 = 0, w1 = 0;
-            int mbase = 0;
-            if (valid && c0 + HALF > Lb) {
-                mbase = max(c0 - Lb, 0) & ~63;
-                const int wi = mbase >> 6;
-                w0 = wi < a.W ? __ldg(mrow + wi) : 0ull;
-                w1 = wi + 1 < a.W ? __ldg(mrow + wi + 1) : 0ull;
-            }
-#pragma unroll
-            for (int i = 0; i < HALF; ++i) {
-                const int key = c0 + i;
-                bool vis = key >= klo && key < k_end;
-                if (key >= Lb) {
-                    const int m = key - Lb - mbase;  // in [0, 96)
-                    vis = vis && valid && (((m < 64 ? w0 >> m : w1 >> (m - 64)) & 1ull) != 0);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t qo = ((ks >> 2) * (kUmmaM * 128) + (ks & 3) * 32) >> 4;
+                    const uint32_t ko = ((ks >> 2) * (kBlockN * 128) + (ks & 3) * 32) >> 4;
+                    mma_bf16(d, dq0 + qo, dk + ko, idesc_s, ks > 0);
                 }
-                sv[i] = vis ? sv[i] * a.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, sv[i]);
-            }
-        }
-        red[half * 128 + r] = mt;
-        // 3. thread 0 issues S_{j+1} (its K tile has landed) and refills K_j's stage
-        if (tid == 0) {
-            if (j + kRingK < ntiles) { load_k(j + kRingK); k_issued = j + kRingK + 1; }
-            if (j + 1 < ntiles && !issue_s(j + 1)) *flag = 1;
-        }
-        bad = __syncthreads_or(!ok) || *flag;  // B1: row maxima exchanged
-        if (bad) break;
-        mt = fmaxf(mt, red[(half ^ 1) * 128 + r]);
-        // 4. move the reference max when it grows by more than the threshold;
-        //    O in TMEM must hold PV_{j-1} before it is rescaled
-        float corr = 1.f;
-        bool rescale = false;
-        if (mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleThreshold)) {
-            if (m_ref != -INFINITY && j > 0) { corr = exp2f(m_ref - mt); rescale = true; }
-            m_ref = mt;
-        }
-        l *= corr;
-        if (__any_sync(0xffffffffu, rescale)) {  // TMEM loads/stores are warp-collective
-            ok = mbar_wait(mbO0 + 8 * ((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1), kWaitCycles);
-            fence_after_sync();
-            if (ok) {
+                commit(s_full0 + 8 * (t & 1));
+                commit(kempty0 + 8 * (t % kRing));
+            };
+            auto issue_pv = [&](int t) {  // O += P_t V_t
+                const uint64_t dv = dv0 + (uint64_t)(((t % kRing) * L::kTile) >> 4);
+                const uint64_t dp = dp0 + (uint64_t)(((t & 1) * L::kP) >> 4);
 #pragma unroll
-                for (int cc = 0; cc < D / 2; cc += 32) {
-                    float ov[32];
-                    const uint32_t ta = tmem + lane_off + half * (D / 2) + cc;
-                    tmem_ld32(ta, ov);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] *= corr;
-                    tmem_st32(ta, ov);
+                for (int ks = 0; ks < kBlockN / 16; ++ks)
+                    mma_bf16(tmem, dp + ((ks * 32) >> 4), dv + ((ks * 2048) >> 4), idesc_pv,
+                             (t > 0 || ks > 0) ? 1u : 0u);
+                commit(o_done0 + 8 * (t & 1));
+                commit(vempty0 + 8 * (t % kRing));
+            };
+            if ((!a.q_tma || wait(qfull, 0)) && wait(kfull0, 0)) issue_s(0);
+            for (int i = 0; i <= ntiles && !fail; ++i) {
+                if (i >= 1) {  // PV of tile i-1 once its P is written and its V has landed
+                    const int t = i - 1;
+                    if (!wait(p_full0 + 8 * (t & 1), (t >> 1) & 1)) break;
+                    if (!wait(vfull0 + 8 * (t % kRing), (t / kRing) & 1)) break;
+                    fence_after_sync();
+                    issue_pv(t);
                 }
-                tmem_wait_st();
+                if (i + 1 < ntiles) {  // S of tile i+1 (its S buffer was read by softmax i-1)
+                    const int t = i + 1;
+                    if (!wait(kfull0 + 8 * (t % kRing), (t / kRing) & 1)) break;
+                    issue_s(t);
+                }
             }
         }
-        // 5. P buffer j & 1 was last read by PV_{j-2}; its V stage is then free
-        if (j >= 2) {
-            ok = mbar_wait(mbO0 + 8 * (j & 1), (uint32_t)(((j - 2) >> 1) & 1), kWaitCycles) && ok;
+    } else if (warp == kTmaWarp) {
+        // -------------------------------- TMA lane --------------------------------
+        if (lane == 0) {
+            int issued = min(kRing, ntiles);  // tiles whose K and V were requested
+            bool fail = false;
+            for (int t = kRing; t < ntiles; ++t) {
+                // stage t % kRing held tile t - kRing: wait for the MMAs that read it
+                const uint32_t par = (uint32_t)((t / kRing - 1) & 1);
+                if (!mbar_wait(kempty0 + 8 * (t % kRing), par, kWaitCycles)) { fail = true; break; }
+                mbar_expect_tx(kfull0 + 8 * (t % kRing), L::kTile);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+                    tma_load_3d(ks_a + (t % kRing) * L::kTile + x * kBlockN * 128, &tmk, x * 64, tile_start(t),
+                                zrow, kfull0 + 8 * (t % kRing));
+                if (!mbar_wait(vempty0 + 8 * (t % kRing), par, kWaitCycles)) {
+                    // K of tile t is in flight: let it land before giving up
+                    mbar_wait(kfull0 + 8 * (t % kRing), (uint32_t)((t / kRing) & 1), kWaitCycles);
+                    fail = true;
+                    break;
+                }
+                mbar_expect_tx(vfull0 + 8 * (t % kRing), L::kTile);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+                    tma_load_3d(vs_a + (t % kRing) * L::kTile + x * kBlockN * 128, &tmv, x * 64, tile_start(t),
+                                zrow, vfull0 + 8 * (t % kRing));
+                issued = t + 1;
+            }
+            if (fail) {
+                *flag = 1;
+                // let the loads in flight land before the CTA can leave
+                for (int t = max(0, issued - kRing); t < issued; ++t) {
+                    mbar_wait(kfull0 + 8 * (t % kRing), (uint32_t)((t / kRing) & 1), kWaitCycles);
+                    mbar_wait(vfull0 + 8 * (t % kRing), (uint32_t)((t / kRing) & 1), kWaitCycles);
+                }
+            }
+        }
+    } else {
+        // ------------------------------ softmax warps ------------------------------
+        const int qi = qrow_of(r);            // query-block row of TMEM lane r, or -1
+        const bool valid = qi >= 0;
+        const int grow = row0 + max(qi, 0);
+        const bool warp_valid = __any_sync(0xffffffffu, valid);
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const int node = valid ? grow / G : 0;
+        const uint64_t* mrow = a.mask + (size_t)node * a.W;
+        bool fail = false;
+        for (int j = 0; j < ntiles; ++j) {
+            bool ok = !fail && mbar_wait(s_full0 + 8 * (j & 1), (uint32_t)((j >> 1) & 1), kWaitCycles);
+            ok = __all_sync(0xffffffffu, ok);
             fence_after_sync();
-            if (tid == 0 && j - 2 + kRingV < ntiles) { load_v(j - 2 + kRingV); v_issued = j - 2 + kRingV + 1; }
-        }
-        const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-        uint8_t* prow = base + L::kOffP + (j & 1) * L::kP;
-        float psum = 0.f;
+            float sv[SW];
+            float mt = -INFINITY;
+            const int kt = tile_start(j), klo = tile_lo(j);
+            if (warp_valid && ok) {
+                tmem_ld16(tmem + lane_off + kSCol + (j & 1) * kBlockN + q * SW, sv);
+                tmem_wait_ld();
+                const int c0 = kt + q * SW;  // key of sv[0]
+                if (kt == klo && kt + kBlockN <= min(k_end, Lb)) {  // plain prefix tile
 #pragma unroll
-        for (int c = 0; c < HALF / 8; ++c) {
-            uint32_t pk[4];
+                    for (int i = 0; i < SW; ++i) { sv[i] *= a.scale_log2; mt = fmaxf(mt, sv[i]); }
+                } else {
+                    uint64_t w0 = 0, w1 = 0;
+                    int mbase = 0;
+                    if (valid && c0 + SW > Lb) {
+                        mbase = max(c0 - Lb, 0) & ~63;
+                        const int wi = mbase >> 6;
+                        w0 = wi < a.W ? __ldg(mrow + wi) : 0ull;
+                        w1 = wi + 1 < a.W ? __ldg(mrow + wi + 1) : 0ull;
+                    }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float p0 = exp2f(sv[c * 8 + 2 * e] - mr);
-                const float p1 = exp2f(sv[c * 8 + 2 * e + 1] - mr);
-                psum += p0 + p1;
-                pk[e] = pack_bf16(p0, p1);
+                    for (int i = 0; i < SW; ++i) {
+                        const int key = c0 + i;
+                        bool vis = key >= klo && key < k_end;
+                        if (key >= Lb) {
+                            const int m = key - Lb - mbase;  // in [0, 80)
+                            vis = vis && valid && (((m < 64 ? w0 >> m : w1 >> (m - 64)) & 1ull) != 0);
+                        }
+                        sv[i] = vis ? sv[i] * a.scale_log2 : -INFINITY;
+                        mt = fmaxf(mt, sv[i]);
+                    }
+                }
             }
-            *reinterpret_cast<uint4*>(prow + sw128_offset(r, half * (HALF / 8) + c, kUmmaM)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            float* rj = red + (j & 1) * 4 * 128;
+            rj[q * 128 + r] = mt;
+            if (named_barrier_or(1, kSoftmaxThreads, !ok)) { fail = true; break; }
+            mt = fmaxf(fmaxf(rj[r], rj[128 + r]), fmaxf(rj[256 + r], rj[384 + r]));
+            float corr = 1.f;
+            bool rescale = false;
+            if (mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleThreshold)) {
+                if (m_ref != -INFINITY && j > 0) { corr = exp2f(m_ref - mt); rescale = true; }
+                m_ref = mt;
+            }
+            l *= corr;
+            if (warp_valid && __any_sync(0xffffffffu, rescale)) {
+                // O must hold PV_{j-1} before it is rescaled (warp-collective TMEM access)
+                ok = mbar_wait(o_done0 + 8 * ((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1), kWaitCycles);
+                ok = __all_sync(0xffffffffu, ok);
+                fence_after_sync();
+                if (ok) {
+                    const uint32_t ta = tmem + lane_off + q * QW;
+                    if constexpr (QW == 32) {
+                        float ov[32];
+                        tmem_ld32(ta, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] *= corr;
+                        tmem_st32(ta, ov);
+                    } else {
+                        float ov[16];
+                        tmem_ld16(ta, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) ov[i] *= corr;
+                        tmem_st16(ta, ov);
+                    }
+                    tmem_wait_st();
+                } else {
+                    fail = true;
+                }
+            }
+            if (warp_valid) {
+                if (j >= 2) {  // P buffer j & 1 was last read by PV_{j-2}
+                    ok = mbar_wait(o_done0 + 8 * (j & 1), (uint32_t)(((j - 2) >> 1) & 1), kWaitCycles);
+                    if (!ok) fail = true;
+                }
+                const float mr = m_ref == -INFINITY ? 0.f : m_ref;
+                uint8_t* prow = base + L::kOffP + (j & 1) * L::kP;
+                float psum = 0.f;
+#pragma unroll
+                for (int c = 0; c < SW / 8; ++c) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float p0 = exp2_approx(sv[c * 8 + 2 * e] - mr);
+                        const float p1 = exp2_approx(sv[c * 8 + 2 * e + 1] - mr);
+                        psum += p0 + p1;
+                        pk[e] = pack_bf16(p0, p1);
+                    }
+                    *reinterpret_cast<uint4*>(prow + sw128_offset(r, q * (SW / 8) + c, kUmmaM)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                l += psum;
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full0 + 8 * (j & 1));
         }
-        l += psum;
-        // 6. P visible to the tensor core, then PV_j
-        fence_async_smem();
-        fence_before_sync();
-        bad = __syncthreads_or(!ok);  // B2
+        bool ok = !fail;
+        if (ok && ntiles > 0)
+            ok = mbar_wait(o_done0 + 8 * ((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1), kWaitCycles);
+        float* rl = red + (ntiles & 1) * 4 * 128;
+        rl[q * 128 + r] = l;
+        bad = named_barrier_or(1, kSoftmaxThreads, !ok);
+        l = rl[r] + rl[128 + r] + rl[256 + r] + rl[384 + r];
         fence_after_sync();
-        if (bad) break;
-        if (tid == 0 && !issue_pv(j)) *flag = 1;
     }
-    // drain: the last PV (and, on failure, whatever is in flight)
-    bool ok = !bad && mbar_wait(mbO0 + 8 * ((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1), kWaitCycles);
-    fence_after_sync();
-    red[half * 128 + r] = l;
-    bad = __syncthreads_or(!ok) || *flag;
-    if (bad && tid == 0) {
-        // give the tensor core and the TMA loads in flight a second bounded
-        // chance to finish before TMEM is freed and the CTA leaves
-        mbar_wait(mbO0 + 8 * ((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1), kWaitCycles);
-        for (int t = max(0, k_issued - kRingK); t < k_issued; ++t)
-            mbar_wait(kfull0 + 8 * (t % kRingK), (uint32_t)((t / kRingK) & 1), kWaitCycles);
-        for (int t = max(0, v_issued - kRingV); t < v_issued; ++t)
-            mbar_wait(vfull0 + 8 * (t % kRingV), (uint32_t)((t / kRingV) & 1), kWaitCycles);
-    }
-    __syncthreads();
-    const float lt = l + red[(half ^ 1) * 128 + r];
+    bad = __syncthreads_or(bad);
+    bad = bad || *flag != 0;  // every write to the flag precedes the barrier
 
-    // epilogue: this thread's half of the O row (TMEM loads are warp-collective)
-    const int hq = hk * G + grow % G;
-    const int S = gridDim.x;
-    float* dst = nullptr;
-    float scale = 1.f;
-    if (valid) {
-        if (S == 1) {
-            dst = a.out + (((size_t)b * N + node) * a.Hq + hq) * D;
-            scale = lt > 0.f ? 1.f / lt : 0.f;
-        } else {
-            const size_t prow = (((size_t)b * a.Hq + hq) * N + node) * S + split;
-            dst = a.part_o + prow * D;
-            if (half == 0) {
-                a.part_ml[prow * 2] = bad ? NAN : m_ref;
-                a.part_ml[prow * 2 + 1] = bad ? NAN : lt;
-            }
-        }
-    }
+    // ------------------------------ epilogue ------------------------------
+    float ov[QW];
 #pragma unroll
-    for (int cc = 0; cc < D / 2; cc += 32) {
-        float ov[32];
-        const int col = half * (D / 2) + cc;
-        tmem_ld32(tmem + lane_off + col, ov);
+    for (int i = 0; i < QW; ++i) ov[i] = 0.f;
+    const int qi = qrow_of(r);
+    const int grow = row0 + max(qi, 0);
+    const bool valid = warp < kSoftmaxWarps && qi >= 0;
+    if (warp < kSoftmaxWarps && __any_sync(0xffffffffu, valid) && ntiles > 0) {
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        if constexpr (QW == 32) tmem_ld32(tmem + lane_off + q * QW, ov);
+        else tmem_ld16(tmem + lane_off + q * QW, ov);
         tmem_wait_ld();
-        if (valid) {
+    }
+    if (S == 1 && valid) {
+        const int node = grow / G, hq = hk * G + grow % G;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float* dst = a.out + (((size_t)b * N + node) * a.Hq + hq) * D + q * QW;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4*>(dst + col + i) =
-                    bad ? make_float4(NAN, NAN, NAN, NAN)
-                        : make_float4(ov[i] * scale, ov[i + 1] * scale, ov[i + 2] * scale, ov[i + 3] * scale);
-        }
+        for (int i = 0; i < QW; i += 4)
+            *reinterpret_cast<float4*>(dst + i) =
+                bad ? make_float4(NAN, NAN, NAN, NAN)
+                    : make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv, ov[i + 3] * inv);
     }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
-}
+    if (S == 1) return;
 
-// One warp per (b, node, query head): merge the splits that hold keys.  Lane s
-// reads split s's (max, sum); the output columns are spread over the lanes and
-// the splits' partial outputs are read four at a time.
-template <int D>
-__global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
-    pdl_wait();
-    pdl_trigger();
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= a.B * a.N * a.Hq) return;
-    const int b = row / (a.N * a.Hq), node = (row / a.Hq) % a.N, hq = row % a.Hq;
-    const int L = clamp_len(a.kv_len[b], a.N, a.Lmax);
-    const int S = a.S;
-    const int active = min(S, (L + a.N + a.chunk - 1) / a.chunk);
-    const size_t prow = (((size_t)b * a.Hq + hq) * a.N + node) * S;
-    // split weights: lane s holds split s (and s + 32, ...)
-    constexpr int kMaxSplitRegs = 2;  // S <= 64
-    float ms[kMaxSplitRegs], ls[kMaxSplitRegs];
-    float mx = -INFINITY;
+    // ------------------ merge the cluster's split partials ------------------
+    // row r belongs to CTA r % S and is its (r / S)-th row; split s of it goes to
+    // slot [s][r / S] of the owner's receive area (the owner's rings, free once
+    // every CTA of the cluster has left its tile loop)
+    const int own_rows = (kUmmaM + S - 1) / S;
+    float* part_o = reinterpret_cast<float*>(base + L::kOffPartO);
+    float* part_ml = reinterpret_cast<float*>(base + L::kOffPartML);
+    cluster_sync();
+    if (valid) {
+        const int owner = qi % S, slot = split * own_rows + qi / S;
+        const uint32_t po = cluster_map(smem_addr(part_o + (size_t)slot * D + q * QW), owner);
 #pragma unroll
-    for (int r = 0; r < kMaxSplitRegs; ++r) {
-        const int s = lane + 32 * r;
-        ms[r] = -INFINITY;
-        ls[r] = 0.f;
-        if (s < active) {
-            const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + (prow + s) * 2);
-            ms[r] = ml.x;
-            ls[r] = ml.y;
-            if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
+        for (int i = 0; i < QW; i += 4)
+            st_cluster_f32x4(po + i * 4, make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]));
+        if (q == 0)
+            st_cluster_f32x2(cluster_map(smem_addr(part_ml + 2 * slot), owner), bad ? NAN : (ntiles > 0 ? m_ref : -INFINITY),
+                             bad ? NAN : (ntiles > 0 ? l : 0.f));
+    }
+    cluster_sync();  // all partials delivered
+    const int me = (int)cluster_rank();
+    const int nvalid = min(rows - row0, kUmmaM);
+    const int nmine = nvalid > me ? (nvalid - me + S - 1) / S : 0;
+    constexpr int C4 = D / 4;
+    for (int idx = tid; idx < nmine * C4; idx += kAttnThreads) {
+        const int lr = idx / C4, c4 = idx % C4;
+        float mx = -INFINITY;
+        bool nan_seen = false;
+        for (int sp = 0; sp < S; ++sp) {
+            const float ls = part_ml[2 * (sp * own_rows + lr) + 1];
+            if (ls != ls) nan_seen = true;
+            else if (ls > 0.f) mx = fmaxf(mx, part_ml[2 * (sp * own_rows + lr)]);
         }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float base = mx == -INFINITY ? 0.f : mx;
-    float wl[kMaxSplitRegs], lsum = 0.f;
-#pragma unroll
-    for (int r = 0; r < kMaxSplitRegs; ++r) {
-        wl[r] = ls[r] > 0.f ? exp2f(ms[r] - base) : 0.f;
-        lsum += ls[r] * wl[r];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-    constexpr int PER = D / 32;
-    float acc[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    for (int s0 = 0; s0 < active; s0 += 4) {
-        float w[4], v[4][PER];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int s = s0 + j;
-            w[j] = __shfl_sync(0xffffffffu, (s >> 5) == 0 ? wl[0] : wl[1], s & 31);
-            const float* src = a.part_o + (prow + min(s, active - 1)) * D;
-#pragma unroll
-            for (int i = 0; i < PER; ++i) v[j][i] = src[lane + 32 * i];
-            if (s >= active) w[j] = 0.f;
+        const float basem = mx == -INFINITY ? 0.f : mx;
+        float lsum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < S; ++sp) {
+            const int slot = sp * own_rows + lr;
+            const float ls = part_ml[2 * slot + 1];
+            if (!(ls > 0.f)) continue;
+            const float w = exp2f(part_ml[2 * slot] - basem);
+            lsum += ls * w;
+            const float4 o = *reinterpret_cast<const float4*>(part_o + (size_t)slot * D + c4 * 4);
+            acc.x += o.x * w; acc.y += o.y * w; acc.z += o.z * w; acc.w += o.w * w;
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int i = 0; i < PER; ++i) acc[i] = fmaf(v[j][i], w[j], acc[i]);
+        const float inv = nan_seen ? NAN : (lsum > 0.f ? 1.f / lsum : 0.f);
+        const int gr = row0 + lr * S + me;
+        const int node = gr / G, hq = hk * G + gr % G;
+        *reinterpret_cast<float4*>(a.out + (((size_t)b * N + node) * a.Hq + hq) * D + c4 * 4) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    float* dst = a.out + (((size_t)b * a.N + node) * a.Hq + hq) * D;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) dst[lane + 32 * i] = acc[i] * inv;
 }
 
 // float32 storage: one warp per (b, node, query head), keys in order, online softmax.
@@ -500,45 +580,36 @@ __global__ void __launch_bounds__(256) tree_attn_f32_kernel(const float* __restr
 }
 
 struct AttnPlan {
-    int qblocks, S, chunk, cps;
-    size_t smem, off_o, off_ml, ws_bytes;
+    int qblocks, S, chunk;
+    size_t smem;
 };
 
 // Splits of the key range: the grid is (S, Hkv * qblocks, B) CTAs of kUmmaM
-// query rows each.  S trades wave quantisation (one CTA per SM) against each
-// CTA's fixed set-up; the split plan assumes the caches are mostly full (keys
-// up to Lmax).
+// query rows each, one CTA per SM; the S CTAs of a (head, query block) form a
+// cluster.  S trades wave quantisation against each CTA's fixed set-up; the
+// split plan assumes the caches are mostly full (keys up to Lmax).
 AttnPlan plan_attention(int B, int N, int Hq, int Hkv, int D, int Lmax) {
     AttnPlan p{};
     const int rows = N * (Hq / Hkv);
     p.qblocks = (rows + kUmmaM - 1) / kUmmaM;
-    p.smem = D == 128 ? (size_t)UmmaSmem<128>::kBytes : (size_t)UmmaSmem<64>::kBytes;
-    p.cps = 1;
+    p.smem = D == 128 ? (size_t)AttnSmem<128>::kBytes : (size_t)AttnSmem<64>::kBytes;
     const long long units = (long long)B * Hkv * p.qblocks;
-    const long long target = (long long)sm_count() * p.cps;
-    const int max_splits = (Lmax + kBlockN - 1) / kBlockN;
-    // cost in tile times: each wave takes the CTA's fixed set-up (about
-    // kSetupTiles tiles: TMEM, barriers, Q, pipeline fill) plus its tiles
+    const long long target = (long long)sm_count();
+    const int max_tiles = (Lmax + kBlockN - 1) / kBlockN;
+    // cost in tile times: each wave takes the CTA's set-up (about kSetupTiles
+    // tiles: TMEM, barriers, Q, pipeline fill) plus its tiles
     constexpr int kSetupTiles = 4;
     int best = 1;
     long long best_cost = -1;
-    for (int s = 1; s <= max_splits && s <= 64; ++s) {  // the combine holds <= 64 splits per row
+    for (int s = 1; s <= max_tiles && s <= kMaxSplits; ++s) {
         const long long waves = (units * s + target - 1) / target;
-        const long long cost = waves * (kSetupTiles + (max_splits + s - 1) / s);
+        const long long cost = waves * (kSetupTiles + (max_tiles + s - 1) / s);
         if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = s; }
     }
     int chunk = (Lmax + best - 1) / best;
     chunk = (chunk + kBlockN - 1) / kBlockN * kBlockN;
     p.chunk = chunk;
     p.S = (Lmax + chunk - 1) / chunk;
-    size_t off = 0;
-    p.off_o = off;
-    if (p.S > 1) {
-        off = align_up(off + (size_t)B * Hq * N * p.S * D * sizeof(float), 256);
-        p.off_ml = off;
-        off = align_up(off + (size_t)B * Hq * N * p.S * 2 * sizeof(float), 256);
-    }
-    p.ws_bytes = off;
     return p;
 }
 
@@ -582,22 +653,57 @@ int kv_tensor_map(CUtensorMap* m, const void* cache, int D, int Lmax, int BH) {
     return MEDUSA_OK;
 }
 
+// q [B][N][Hq][D] as a 4-D tensor (D, Hq, N, B); a box of 64 x G x (box_rows/G)
+// x 1 holds box_rows consecutive rows (node, group member) of a query block.
+int q_tensor_map(CUtensorMap* m, const void* q, int D, int Hq, int N, int B, int G, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return fail(MEDUSA_ERR_CUDA, "tree_attention: cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)N, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2, (cuuint64_t)N * Hq * D * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)(box_rows / G), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MEDUSA_ERR_CUDA, "tree_attention: q tensor map encode failed (%d)", (int)r);
+    return MEDUSA_OK;
+}
+
 template <int D>
 int launch_bf16(AttnArgs& a, const AttnPlan& p, cudaStream_t st) {
-    CUtensorMap tmk, tmv;
+    CUtensorMap tmk, tmv, tmq;
     int rc = kv_tensor_map(&tmk, a.k, D, a.Lmax, a.B * a.Hkv);
     if (rc) return rc;
     rc = kv_tensor_map(&tmv, a.v, D, a.Lmax, a.B * a.Hkv);
     if (rc) return rc;
-    dim3 grid(p.S, a.Hkv * p.qblocks, a.B);
+    const int rows = a.N * a.G;
+    a.spread = rows <= kUmmaM / 2 ? 1 : 0;
+    const int box_rows = a.spread ? 16 : kUmmaM;  // rows per TMA box
+    a.q_tma = (a.G <= box_rows && box_rows % a.G == 0) ? 1 : 0;
+    if (a.q_tma) {
+        rc = q_tensor_map(&tmq, a.q, D, a.Hq, a.N, a.B, a.G, box_rows);
+        if (rc) return rc;
+    } else {
+        tmq = tmk;  // unused
+    }
     auto kern = tree_attn_umma_kernel<D>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-    cudaError_t e = launch(kern, grid, dim3(kUmmaThreads), p.smem, st, tmk, tmv, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.S, a.Hkv * p.qblocks, a.B);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = p.S;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmk, tmv, tmq, a);
     if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "tree_attention: launch failed: %s", cudaGetErrorString(e));
-    if (p.S == 1) return MEDUSA_OK;
-    const int rows = a.B * a.N * a.Hq;
-    e = launch(attn_combine_kernel<D>, dim3((rows + 7) / 8), dim3(256), 0, st, a);
-    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "attn_combine: launch failed: %s", cudaGetErrorString(e));
     return MEDUSA_OK;
 }
 
@@ -607,8 +713,8 @@ int launch_bf16(AttnArgs& a, const AttnPlan& p, cudaStream_t st) {
 using namespace medusa;
 
 extern "C" size_t medusa_tree_attention_workspace(int B, int N, int Hq, int Hkv, int D, int Lmax) {
-    if (check_attn(B, N, Hq, Hkv, D, Lmax)) return 0;
-    return plan_attention(B, N, Hq, Hkv, D, Lmax).ws_bytes;
+    (void)B; (void)N; (void)Hq; (void)Hkv; (void)D; (void)Lmax;
+    return 0;  // split partials are merged on chip (thread-block cluster)
 }
 
 extern "C" int medusa_tree_attention(const void* q, const void* k_cache, const void* v_cache,
@@ -636,12 +742,11 @@ extern "C" int medusa_tree_attention(const void* q, const void* k_cache, const v
     }
     if (dtype != MEDUSA_BF16)
         return fail(MEDUSA_ERR_UNSUPPORTED, "tree_attention: unknown dtype %d", (int)dtype);
+    (void)ws;
+    (void)ws_bytes;
     AttnPlan p = plan_attention(B, N, Hq, Hkv, D, Lmax);
-    if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes))
-        return fail(MEDUSA_ERR_WORKSPACE, "tree_attention: workspace of %zu bytes needed, %zu given",
-                    p.ws_bytes, ws ? ws_bytes : (size_t)0);
-    if (p.ws_bytes > 0 && !aligned16(ws))
-        return fail(MEDUSA_ERR_INVALID_ARG, "tree_attention: ws must be 16-byte aligned");
+    if (p.smem > (size_t)max_smem_optin())
+        return fail(MEDUSA_ERR_UNSUPPORTED, "tree_attention: %zu bytes of shared memory needed", p.smem);
     AttnArgs a{};
     a.q = (const uint16_t*)q;
     a.k = (const uint16_t*)k_cache;
@@ -649,8 +754,6 @@ extern "C" int medusa_tree_attention(const void* q, const void* k_cache, const v
     a.kv_len = kv_len;
     a.mask = mask;
     a.out = out;
-    a.part_o = p.S > 1 ? (float*)((char*)ws + p.off_o) : nullptr;
-    a.part_ml = p.S > 1 ? (float*)((char*)ws + p.off_ml) : nullptr;
     a.B = B; a.N = N; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.Lmax = Lmax; a.W = W;
     a.S = p.S; a.chunk = p.chunk; a.qblocks = p.qblocks;
     a.scale_log2 = scale * kLog2e;
