@@ -27,7 +27,7 @@
 namespace medusa {
 namespace {
 
-constexpr int kBlockN = 64;  // keys per tile
+constexpr int kBlockN = 128;  // keys per tile
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -70,18 +70,19 @@ __device__ __forceinline__ int clamp_len(int L, int N, int Lmax) {
 // that all four SM sub-partitions share the softmax.
 //
 // Warp roles (576 threads):
-//   warps 0-15  softmax: thread (r, q), q = tid / 128, owns 16 of the 64
+//   warps 0-15  softmax: thread (r, q), q = tid / 128, owns 32 of the 128
 //               scores of TMEM lane r in every tile and D/4 of its output
 //               columns; the four owners of a row exchange their maxima
 //               through shared memory (one named barrier per tile)
 //   warp 16     MMA: lane 0 issues every tcgen05.mma and commit
-//   warp 17     TMA: lane 0 loads Q and streams K and V tiles into two 4-deep
+//   warp 17     TMA: lane 0 loads Q and streams K and V tiles into two 2-deep
 //               rings
-// Per 64-key tile j (keys [k_j, k_j + 64)):
+// Per 128-key tile j (keys [k_j, k_j + 128)):
 //   S_j = Q K_j^T       tcgen05.mma into TMEM S buffer j & 1      (s_full)
-//   softmax             row max, P_j = exp2(S_j*scale*log2e - m) as bf16 into
-//                       swizzled P buffer j & 1                 (p_full)
-//   O += P_j V_j        tcgen05.mma into the TMEM accumulator    (o_done)
+//   softmax             row max, P_j = exp2(S_j*scale*log2e - m) as bf16
+//                       written back over S buffer j & 1        (p_full)
+//   O += P_j V_j        tcgen05.mma, A = P_j from TMEM, into the TMEM
+//                       accumulator                             (o_done)
 // The MMA lane issues PV_{j-1} and S_{j+1} while the softmax warps work on tile
 // j.  Every ring stage has a full barrier (TMA bytes landed) and an empty
 // barrier (the MMA that read it completed), so no wait can fall two phases
@@ -100,7 +101,7 @@ constexpr int kSoftmaxWarps = 16;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
 constexpr int kAttnThreads = kSoftmaxThreads + 64;
-constexpr int kRing = 4;       // K and V ring depth
+constexpr int kRing = 2;       // K and V ring depth
 constexpr int kMaxSplits = 8;  // portable cluster size
 constexpr float kRescaleThreshold = 8.f;
 constexpr long long kWaitCycles = 1ll << 31;  // ~1 s at 2 GHz
@@ -109,11 +110,9 @@ template <int D>
 struct AttnSmem {
     static constexpr int kQ = kUmmaM * D * 2;
     static constexpr int kTile = kBlockN * D * 2;  // one K or V tile
-    static constexpr int kP = kUmmaM * kBlockN * 2;
     static constexpr int kOffK = kQ;
     static constexpr int kOffV = kOffK + kRing * kTile;
-    static constexpr int kOffP = kOffV + kRing * kTile;
-    static constexpr int kOffRed = kOffP + 2 * kP;            // float [2][4][128]
+    static constexpr int kOffRed = kOffV + kRing * kTile;     // float [2][4][128]
     static constexpr int kOffBar = kOffRed + 2 * 4 * 128 * 4;
     // kfull[4] vfull[4] kempty[4] vempty[4] s_full[2] o_done[2] p_full[2] qfull
     static constexpr int kNumBar = 4 * kRing + 7;
@@ -133,9 +132,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
     using namespace umma;
     using L = AttnSmem<D>;
     constexpr int CH = D / 8;          // 16-byte chunks per row
-    constexpr int TMEM_COLS = 256;     // O: D columns at 0; S buffers at 128 and 192
+    constexpr int TMEM_COLS = 512;     // O: D columns at 0; S buffers at 128 and 256
     constexpr uint32_t kSCol = 128;
-    constexpr int SW = kBlockN / 4;    // scores per softmax thread
+    constexpr int SW = kBlockN / 4;    // scores per softmax thread (32)
     constexpr int QW = D / 4;          // output columns per softmax thread
     extern __shared__ uint8_t smem_raw[];
 
@@ -143,6 +142,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
     const int hk = blockIdx.y / a.qblocks, qb = blockIdx.y % a.qblocks;
     const int b = blockIdx.z;
     const int N = a.N, G = a.G;
+    if (threadIdx.x == kTmaWarp * 32) {
+        // Warm L2 with this split's first K and V tiles while the previous kernel
+        // finishes.  The rows come from the split's nominal range (no input is
+        // read before the dependency wait); a prefetch is only a hint.
+        const size_t head = ((size_t)b * a.Hkv + hk) * a.Lmax;
+        for (int t = 0; t < kRing; ++t) {
+            const int key0 = split * a.chunk + t * kBlockN;
+            if (key0 >= a.Lmax) break;
+            const uint32_t bytes = (uint32_t)min(kBlockN, a.Lmax - key0) * D * 2;
+            prefetch_l2_bulk(a.k + (head + key0) * D, bytes);
+            prefetch_l2_bulk(a.v + (head + key0) * D, bytes);
+        }
+    }
     pdl_wait();
     pdl_trigger();
     const int Lb = clamp_len(a.kv_len[b], N, a.Lmax);
@@ -167,8 +179,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
     const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
     uint8_t* base = smem_raw + pad;
     const uint32_t base_a = smem_addr(base);
-    const uint32_t qs_a = base_a, ks_a = base_a + L::kOffK, vs_a = base_a + L::kOffV,
-                   ps_a = base_a + L::kOffP;
+    const uint32_t qs_a = base_a, ks_a = base_a + L::kOffK, vs_a = base_a + L::kOffV;
     float* red = reinterpret_cast<float*>(base + L::kOffRed);
     const uint32_t bar_a = base_a + L::kOffBar;
     const uint32_t kfull0 = bar_a, vfull0 = kfull0 + 8 * kRing, kempty0 = vfull0 + 8 * kRing,
@@ -247,7 +258,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
             // to the start-address field
             const uint64_t dq0 = desc_sw128(qs_a, 16, 1024);
             const uint64_t dk0 = desc_sw128(ks_a, 16, 1024);
-            const uint64_t dp0 = desc_sw128(ps_a, 16, 1024);
             const uint64_t dv0 = desc_sw128(vs_a, kBlockN * 128, 1024);
             bool fail = false;
             auto wait = [&](uint32_t bar, uint32_t parity) {
@@ -267,13 +277,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
                 commit(s_full0 + 8 * (t & 1));
                 commit(kempty0 + 8 * (t % kRing));
             };
-            auto issue_pv = [&](int t) {  // O += P_t V_t
+            auto issue_pv = [&](int t) {  // O += P_t V_t, P_t in TMEM over S buffer t & 1
                 const uint64_t dv = dv0 + (uint64_t)(((t % kRing) * L::kTile) >> 4);
-                const uint64_t dp = dp0 + (uint64_t)(((t & 1) * L::kP) >> 4);
+                const uint32_t pa = tmem + kSCol + (t & 1) * kBlockN;
 #pragma unroll
                 for (int ks = 0; ks < kBlockN / 16; ++ks)
-                    mma_bf16(tmem, dp + ((ks * 32) >> 4), dv + ((ks * 2048) >> 4), idesc_pv,
-                             (t > 0 || ks > 0) ? 1u : 0u);
+                    mma_bf16_ta(tmem, pa + ks * 8, dv + ((ks * 2048) >> 4), idesc_pv,
+                                (t > 0 || ks > 0) ? 1u : 0u);
                 commit(o_done0 + 8 * (t & 1));
                 commit(vempty0 + 8 * (t % kRing));
             };
@@ -347,7 +357,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
             float mt = -INFINITY;
             const int kt = tile_start(j), klo = tile_lo(j);
             if (warp_valid && ok) {
-                tmem_ld16(tmem + lane_off + kSCol + (j & 1) * kBlockN + q * SW, sv);
+                tmem_ld32(tmem + lane_off + kSCol + (j & 1) * kBlockN + q * SW, sv);
                 tmem_wait_ld();
                 const int c0 = kt + q * SW;  // key of sv[0]
                 if (kt == klo && kt + kBlockN <= min(k_end, Lb)) {  // plain prefix tile
@@ -367,7 +377,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
                         const int key = c0 + i;
                         bool vis = key >= klo && key < k_end;
                         if (key >= Lb) {
-                            const int m = key - Lb - mbase;  // in [0, 80)
+                            const int m = key - Lb - mbase;  // in [0, 96)
                             vis = vis && valid && (((m < 64 ? w0 >> m : w1 >> (m - 64)) & 1ull) != 0);
                         }
                         sv[i] = vis ? sv[i] * a.scale_log2 : -INFINITY;
@@ -414,29 +424,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
                 }
             }
             if (warp_valid) {
-                if (j >= 2) {  // P buffer j & 1 was last read by PV_{j-2}
-                    ok = mbar_wait(o_done0 + 8 * (j & 1), (uint32_t)(((j - 2) >> 1) & 1), kWaitCycles);
-                    if (!ok) fail = true;
-                }
+                // P_j (bf16, two per column) over the first 32 columns of S buffer
+                // j & 1: every owner has read its scores before the barrier above
                 const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-                uint8_t* prow = base + L::kOffP + (j & 1) * L::kP;
+                uint32_t pk[SW / 2];
                 float psum = 0.f;
 #pragma unroll
-                for (int c = 0; c < SW / 8; ++c) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p0 = exp2_approx(sv[c * 8 + 2 * e] - mr);
-                        const float p1 = exp2_approx(sv[c * 8 + 2 * e + 1] - mr);
-                        psum += p0 + p1;
-                        pk[e] = pack_bf16(p0, p1);
-                    }
-                    *reinterpret_cast<uint4*>(prow + sw128_offset(r, q * (SW / 8) + c, kUmmaM)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                for (int e = 0; e < SW / 2; ++e) {
+                    const float p0 = exp2_approx(sv[2 * e] - mr);
+                    const float p1 = exp2_approx(sv[2 * e + 1] - mr);
+                    psum += p0 + p1;
+                    pk[e] = pack_bf16(p0, p1);
                 }
+                tmem_st16u(tmem + lane_off + kSCol + (j & 1) * kBlockN + q * (SW / 2), pk);
+                tmem_wait_st();
                 l += psum;
             }
-            fence_async_smem();
+            fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full0 + 8 * (j & 1));
         }
