@@ -238,7 +238,8 @@ int medusa_verify_accept_chain(const float* p, const float* q, const int32_t* dr
 /*   src_idx [B,Dmax+1] out, may be NULL: the source slot of each kept row,   */
 /*   -1 padded.  A sequence whose accept_len, path or L_b is out of range is  */
 /*   left unchanged and its src_idx row is set to -2.                         */
-/* Limits: (D * element size) % 16 == 0.                                     */
+/* Limits: (D * element size) % 16 == 0; (Dmax + 1) * D * element size is at */
+/* most 48 KB; B <= 65535.                                                   */
 /* ------------------------------------------------------------------------- */
 int medusa_kv_compact(void* k_cache, void* v_cache, int32_t* kv_len, const int32_t* path_nodes,
                       const int32_t* accept_len, const int32_t* best_node,

@@ -8,7 +8,7 @@
 // bytes, so the bf16 kernel reads each KV tile once per (sequence, KV head,
 // block of 128 tree queries) and scores all of the block's queries against it
 // on the fifth-generation tensor cores (tcgen05, accumulators in TMEM):
-//   tree_attn_umma_kernel : split-KV over a cluster of CTAs; per 64-key tile
+//   tree_attn_umma_kernel : split-KV over a cluster of CTAs; per 128-key tile
 //                           S = Q K^T and O += P V as tcgen05.mma (bf16 in,
 //                           float32 out) fed by TMA; online softmax in float32;
 //                           ancestor bits tested only on tiles that reach the

@@ -6,16 +6,20 @@
 // L_b .. L_b + a so the cache holds the accepted text in order.  A row's
 // destination can be the source of a later row of the same head, so each block
 // first reads every row it moves into shared memory and only then writes.
-//   kv_compact_kernel : one block per sequence: moves the rows head chunk by
-//                       head chunk, gathers h_next, writes the source slots and
-//                       advances kv_len[b]
+//   kv_compact_kernel : a cluster of CTAs per sequence; each CTA moves the rows
+//                       of its share of the (cache, KV head) pairs, all of a
+//                       pair's rows read before any is written, and gathers its
+//                       share of h_next; after a cluster barrier (every CTA has
+//                       read kv_len[b]) rank 0 advances kv_len[b]
 #include "common.cuh"
+#include "umma.cuh"
 
 namespace medusa {
 namespace {
 
-constexpr int kCompactThreads = 512;
-constexpr size_t kCompactSmem = 64 * 1024;  // staging buffer per block
+constexpr int kCompactThreads = 256;
+constexpr int kCompactCtas = 8;              // CTAs per sequence: one portable cluster
+constexpr size_t kCompactSmem = 48 * 1024;   // staging buffer per CTA
 
 // true iff sequence b's inputs are in range (otherwise it is left unchanged)
 __device__ __forceinline__ bool seq_ok(const int32_t* kv_len, const int32_t* path_nodes,
@@ -30,10 +34,10 @@ __device__ __forceinline__ bool seq_ok(const int32_t* kv_len, const int32_t* pat
     return true;
 }
 
-// One block per sequence.  Heads are moved in chunks that fit the staging
-// buffer: every row of a chunk is read before any is written.  The block then
-// gathers h_next, writes the source slots and finally advances kv_len[b] (no
-// other block reads it).
+// Grid (C, B), cluster (C, 1, 1): CTA r of sequence b owns the (cache, KV head)
+// pairs [r*2Hkv/C, (r+1)*2Hkv/C), moved in chunks that fit the staging buffer.
+// Rows of different pairs never overlap, so only the rows of one pair need to
+// be read before any of them is written.
 __global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(
     uint4* __restrict__ kc, uint4* __restrict__ vc, int32_t* __restrict__ kv_len,
     const int32_t* __restrict__ path_nodes, const int32_t* __restrict__ accept_len,
@@ -41,50 +45,58 @@ __global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(
     uint4* __restrict__ h_next, int Hkv, int row16, int Lmax, int N, int h16, int Dmax,
     int32_t* __restrict__ src_idx) {
     extern __shared__ uint4 buf[];
-    __shared__ int s_ok, s_a, s_L;
+    __shared__ int s_ok, s_a, s_L, s_best;
     pdl_wait();
     pdl_trigger();
-    const int b = blockIdx.x;
+    const int b = blockIdx.y, rank = blockIdx.x, C = gridDim.x;
     if (threadIdx.x == 0) {
         s_ok = seq_ok(kv_len, path_nodes, accept_len, best_node, b, N, Lmax, Dmax);
         s_a = accept_len[b];
         s_L = kv_len[b];
+        s_best = best_node[b];
     }
     __syncthreads();
     const bool ok = s_ok;
     const int a = s_a, L = s_L;
     const int32_t* path = path_nodes + (size_t)b * (Dmax + 1);
-    if (src_idx)
+    if (src_idx && rank == 0)
         for (int i = threadIdx.x; i <= Dmax; i += blockDim.x)
             src_idx[(size_t)b * (Dmax + 1) + i] = !ok ? -2 : (i <= a ? L + path[i] : -1);
-    if (!ok) return;
-    if (hidden_tree && h_next) {
-        const uint4* src = hidden_tree + ((size_t)b * N + best_node[b]) * h16;
-        for (int i = threadIdx.x; i < h16; i += blockDim.x) h_next[(size_t)b * h16 + i] = src[i];
-    }
-    const int per_head = (a + 1) * row16;  // uint4 per head per cache
-    const int cap_heads = max(1, (int)(kCompactSmem / sizeof(uint4)) / (2 * per_head));
-    for (int h0 = 0; h0 < Hkv; h0 += cap_heads) {
-        const int nh = min(cap_heads, Hkv - h0);
-        const int per_cache = nh * per_head;
-        for (int t = threadIdx.x; t < 2 * per_cache; t += blockDim.x) {
-            const int c = t / per_cache, r = t % per_cache;
-            const int h = r / per_head, i = (r / row16) % (a + 1), e = r % row16;
-            const uint4* cache = c ? vc : kc;
-            const size_t row = ((size_t)b * Hkv + h0 + h) * Lmax + L + path[i];
-            buf[t] = cache[row * row16 + e];
+    if (ok) {
+        if (hidden_tree && h_next) {
+            const uint4* src = hidden_tree + ((size_t)b * N + s_best) * h16;
+            const int e0 = rank * h16 / C, e1 = (rank + 1) * h16 / C;
+            for (int i = e0 + threadIdx.x; i < e1; i += blockDim.x) h_next[(size_t)b * h16 + i] = src[i];
         }
-        __syncthreads();
-        for (int t = threadIdx.x; t < 2 * per_cache; t += blockDim.x) {
-            const int c = t / per_cache, r = t % per_cache;
-            const int h = r / per_head, i = (r / row16) % (a + 1), e = r % row16;
-            uint4* cache = c ? vc : kc;
-            const size_t row = ((size_t)b * Hkv + h0 + h) * Lmax + L + i;
-            cache[row * row16 + e] = buf[t];
+        const int pairs = 2 * Hkv;
+        const int p0 = rank * pairs / C, p1 = (rank + 1) * pairs / C;
+        const int per_pair = (a + 1) * row16;  // uint4 per (cache, head)
+        const int cap = max(1, (int)(kCompactSmem / sizeof(uint4)) / per_pair);
+        for (int q0 = p0; q0 < p1; q0 += cap) {
+            const int n = min(cap, p1 - q0) * per_pair;
+#pragma unroll 4
+            for (int t = threadIdx.x; t < n; t += blockDim.x) {
+                const int pr = q0 + t / per_pair, r = t % per_pair;
+                const int c = pr / Hkv, h = pr - c * Hkv, i = r / row16, e = r - i * row16;
+                const uint4* cache = c ? vc : kc;
+                const size_t row = ((size_t)b * Hkv + h) * Lmax + L + path[i];
+                buf[t] = cache[row * row16 + e];
+            }
+            __syncthreads();
+#pragma unroll 4
+            for (int t = threadIdx.x; t < n; t += blockDim.x) {
+                const int pr = q0 + t / per_pair, r = t % per_pair;
+                const int c = pr / Hkv, h = pr - c * Hkv, i = r / row16, e = r - i * row16;
+                uint4* cache = c ? vc : kc;
+                const size_t row = ((size_t)b * Hkv + h) * Lmax + L + i;
+                cache[row * row16 + e] = buf[t];
+            }
+            __syncthreads();
         }
-        __syncthreads();
     }
-    if (threadIdx.x == 0) kv_len[b] = L + a + 1;
+    // kv_len[b] changes only after every CTA of the sequence has read it
+    umma::cluster_sync();
+    if (ok && rank == 0 && threadIdx.x == 0) kv_len[b] = L + a + 1;
 }
 
 }  // namespace
@@ -111,13 +123,15 @@ extern "C" int medusa_kv_compact(void* k_cache, void* v_cache, int32_t* kv_len,
     if (!aligned16(k_cache) || !aligned16(v_cache) || (hidden_tree && (!aligned16(hidden_tree) || !aligned16(h_next))))
         return fail(MEDUSA_ERR_INVALID_ARG, "kv_compact: caches and hidden states must be 16-byte aligned");
     const int row16 = D * elem / 16;
-    if ((size_t)2 * (Dmax + 1) * row16 * sizeof(uint4) > kCompactSmem)
+    if ((size_t)(Dmax + 1) * row16 * sizeof(uint4) > kCompactSmem)
         return fail(MEDUSA_ERR_UNSUPPORTED, "kv_compact: Dmax %d with D %d does not fit the staging buffer",
                     Dmax, D);
+    if (B > 65535) return fail(MEDUSA_ERR_UNSUPPORTED, "kv_compact: batch %d above 65535", B);
     cudaStream_t st = as_stream(stream);
     cudaFuncSetAttribute(kv_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCompactSmem);
-    cudaError_t e = launch(kv_compact_kernel, dim3(B), dim3(kCompactThreads), kCompactSmem, st,
-                           static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), kv_len,
+    cudaError_t e = launch_cluster(kv_compact_kernel, dim3(kCompactCtas, B), dim3(kCompactThreads),
+                                   kCompactSmem, st, kCompactCtas,
+                                   static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), kv_len,
                            path_nodes, accept_len, best_node, static_cast<const uint4*>(hidden_tree),
                            static_cast<uint4*>(h_next), Hkv, row16, Lmax, N,
                            hidden_tree ? H * elem / 16 : 0, Dmax, src_idx);

@@ -112,9 +112,33 @@ __device__ __forceinline__ void dot_rows(const WT* __restrict__ W, int row0, int
     }
 }
 
+// dst[0..8) = the eight bf16 values of w, or dst[0..4) = the four floats of w
+template <typename WT>
+__device__ __forceinline__ void store_chunk(const uint4& w, float* dst);
+template <>
+__device__ __forceinline__ void store_chunk<uint16_t>(const uint4& w, float* dst) {
+    reinterpret_cast<float4*>(dst)[0] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+    reinterpret_cast<float4*>(dst)[1] = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+}
+template <>
+__device__ __forceinline__ void store_chunk<float>(const uint4& w, float* dst) {
+    *reinterpret_cast<float4*>(dst) =
+        make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w));
+}
+
+// dst[0..n) = src[0..n) as float32, with 16-byte loads when src is aligned
+// (n is a multiple of 8, dst 16-byte aligned).  The loads are cached in L2 only:
+// src may have been written by the previous kernel on the stream.
 template <typename WT>
 __device__ __forceinline__ void load_vector_to_smem(const WT* src, float* dst, int n) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = load_scalar<WT>(src, i);
+    constexpr int VEC = Elems<WT>::n;
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll 4
+        for (int c = threadIdx.x; c < n / VEC; c += blockDim.x) store_chunk<WT>(__ldcg(s4 + c), dst + c * VEC);
+    } else {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = load_scalar<WT>(src, i);
+    }
 }
 
 // K1: z[b,k,i] = h[b,i] + SiLU(sum_j W1[k,i,j] h[b,j] + b1[k,i]).
@@ -210,9 +234,15 @@ __global__ void __launch_bounds__(THREADS) heads_w2_topk_kernel(
             prefetch_l2_bulk(wk + (size_t)v0 * H, (uint32_t)bytes);
     }
     pdl_wait();
-    for (int i = threadIdx.x; i < NB * H; i += THREADS) {
-        const int b = i / H, j = i - b * H;
-        xs[i] = z[((size_t)b * K + k) * H + j];
+    {
+        // z rows are 16-byte aligned (H % 8 == 0); L2-only loads, K1 wrote them
+        const int h4 = H / 4;
+#pragma unroll 4
+        for (int c = threadIdx.x; c < NB * h4; c += THREADS) {
+            const int b = c / h4, j = c - b * h4;
+            reinterpret_cast<float4*>(xs)[c] =
+                __ldcg(reinterpret_cast<const float4*>(z + ((size_t)b * K + k) * H) + j);
+        }
     }
     __syncthreads();
     pdl_trigger();
