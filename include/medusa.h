@@ -198,6 +198,32 @@ int medusa_verify_accept_tree(const float* logits, const int32_t* cand, const in
                               size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* 4c. Verification projection fused with tree acceptance  [MH, "Tree         */
+/*     attention and acceptance": the base model scores every branch of the   */
+/*     tree in one pass]                                                      */
+/*                                                                           */
+/* Same outputs and rules as medusa_verify_accept_tree, but the verifier      */
+/* logits are defined from the base model's last hidden state at each tree    */
+/* node: logits[b,u,:] = lm_head . hidden_tree[b,u,:] (bf16 inputs, float32   */
+/* accumulation).  The [B,N,V] logits are never written to memory: the       */
+/* product runs on the tensor cores and is reduced tile by tile into per-row  */
+/* argmax and softmax/entropy statistics.  Typical acceptance computes the    */
+/* candidate logits it needs as separate float32 dot products.                */
+/*   hidden_tree [B,N,H] bf16; lm_head [V,H] bf16 ([out, in]); 16-byte aligned */
+/*   cand [B,N]; parent, depth [N]; outputs as in 4a.                         */
+/* Limits: dtype MEDUSA_BF16; H % 8 == 0, H <= 65536; N <= 512; V <= 2^24.    */
+/* If a device-side wait gives up (about one second), every output of the    */
+/* call is -1.                                                               */
+/* ------------------------------------------------------------------------- */
+size_t medusa_verify_project_workspace(int B, int N, int H, int V);
+int medusa_verify_project_tree(const void* hidden_tree, const void* lm_head, medusa_dtype dtype,
+                               const int32_t* cand, const int32_t* parent, const int32_t* depth,
+                               int B, int N, int H, int V, int Dmax, medusa_accept_mode mode,
+                               float temperature, float eps, float delta, int32_t* accept_len,
+                               int32_t* best_node, int32_t* path_nodes, int32_t* next_tok,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* 4b. Speculative-sampling acceptance along a chain of gamma drafts          */
 /*     [SD, "Faster without changing the result"; "Why a round always yields  */
 /*     exactly k + 1 tokens"]                                                  */

@@ -21,6 +21,7 @@ EXPORTS = (
     "medusa_sparse_tree_paths", "medusa_tree_layout", "medusa_build_tree",
     "medusa_tree_attention_workspace", "medusa_tree_attention",
     "medusa_verify_accept_workspace", "medusa_verify_accept_tree",
+    "medusa_verify_project_workspace", "medusa_verify_project_tree",
     "medusa_verify_chain_workspace", "medusa_verify_accept_chain",
     "medusa_kv_compact",
 )
@@ -60,6 +61,10 @@ def lib() -> C.CDLL:
     L.medusa_verify_accept_workspace.restype = sz
     L.medusa_verify_accept_tree.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, f32, f32,
                                             P, P, P, P, P, sz, P]
+    L.medusa_verify_project_workspace.argtypes = [i32] * 4
+    L.medusa_verify_project_workspace.restype = sz
+    L.medusa_verify_project_tree.argtypes = [P, P, i32, P, P, P, i32, i32, i32, i32, i32, i32, f32,
+                                             f32, f32, P, P, P, P, P, sz, P]
     L.medusa_verify_chain_workspace.argtypes = [i32] * 3
     L.medusa_verify_chain_workspace.restype = sz
     L.medusa_verify_accept_chain.argtypes = [P, P, P, i32, i32, i32, u64, u64, P, P, P, sz, P]

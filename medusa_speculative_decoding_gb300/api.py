@@ -197,6 +197,40 @@ def verify_accept_tree(logits, cand, parent, depth, max_depth, mode="greedy", te
     return out
 
 
+def verify_project_workspace(B, N, H, V):
+    return int(lib().medusa_verify_project_workspace(B, N, H, V))
+
+
+def verify_project_tree(hidden_tree, lm_head, cand, parent, depth, max_depth, mode="greedy",
+                        temperature=1.0, eps=0.09, delta=0.3, out=None, ws=None, stream=None):
+    """verify_accept_tree with the verifier logits defined as lm_head . hidden_tree,
+    computed and reduced on the GPU without materialising them."""
+    _need(hidden_tree, "hidden_tree", torch.bfloat16)
+    _need(lm_head, "lm_head", torch.bfloat16)
+    _need(cand, "cand", torch.int32)
+    _need(parent, "parent", torch.int32)
+    _need(depth, "depth", torch.int32)
+    B, N, H = hidden_tree.shape
+    V = lm_head.shape[0]
+    dev = hidden_tree.device
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   best_node=torch.empty(B, dtype=torch.int32, device=dev),
+                   path_nodes=torch.empty((B, max_depth + 1), dtype=torch.int32, device=dev),
+                   next_tok=torch.empty(B, dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = _ws(verify_project_workspace(B, N, H, V), dev)
+    m = {"greedy": GREEDY, "typical": TYPICAL}[mode]
+    check(lib().medusa_verify_project_tree(_ptr(hidden_tree), _ptr(lm_head), _dtype_of(hidden_tree),
+                                           _ptr(cand), _ptr(parent), _ptr(depth), B, N, H, V,
+                                           max_depth, m, float(temperature), float(eps),
+                                           float(delta), _ptr(out["accept_len"]),
+                                           _ptr(out["best_node"]), _ptr(out["path_nodes"]),
+                                           _ptr(out["next_tok"]), _ptr(ws), ws.numel(),
+                                           _stream(stream)))
+    return out
+
+
 def verify_chain_workspace(B, gamma, V):
     return int(lib().medusa_verify_chain_workspace(B, gamma, V))
 

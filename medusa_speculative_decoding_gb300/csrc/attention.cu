@@ -22,6 +22,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tmap.cuh"
 #include "umma.cuh"
 
 namespace medusa {
@@ -625,20 +626,6 @@ int check_attn(int B, int N, int Hq, int Hkv, int D, int Lmax) {
                     "tree_attention: unsupported shape (N=%d Hq=%d Hkv=%d D=%d Lmax=%d)", N, Hq,
                     Hkv, D, Lmax);
     return MEDUSA_OK;
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
 }
 
 // [B*Hkv][Lmax][D] bf16 cache as a 3-D tensor, boxes of 64 keys x 64 elements,

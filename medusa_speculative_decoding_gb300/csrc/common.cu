@@ -1,10 +1,11 @@
-// common.cu -- status messages and cached device properties.
+// common.cu -- status messages, cached device properties, the tensor-map encoder.
 #include <stdarg.h>
 #include <stdio.h>
 
 #include <mutex>
 
 #include "common.cuh"
+#include "tmap.cuh"
 
 namespace medusa {
 
@@ -61,6 +62,20 @@ int max_smem_optin() {
         g_smem[d] = v;
     }
     return g_smem[d];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
 }
 
 }  // namespace medusa

@@ -9,7 +9,9 @@
 //                        (max, sum exp, sum exp * x) of x = logit / T
 //   accept_tree_kernel : per sequence: merge chunk stats, test each candidate
 //                        against its parent's row, AND along ancestors, pick the
-//                        deepest accepted node (lowest index on ties)
+//                        deepest accepted node (lowest index on ties); also the
+//                        second kernel of the fused verification projection
+//                        (project.cu)
 //
 // Chain (speculative-decoding e-book page, "Faster without changing the
 // result"; "Why a round always yields exactly k + 1 tokens"): accept draft x
@@ -24,31 +26,13 @@
 #include <limits.h>
 
 #include "common.cuh"
+#include "verify_common.cuh"
 
 namespace medusa {
 namespace {
 
 constexpr int kChunk = 4096;     // vocab entries per stats CTA
 constexpr int kStatThreads = 256;
-
-struct RowStat {      // per (row, chunk)
-    float maxv;       // largest logit
-    int arg;          // its lowest index
-    float m, s, a;    // x = logit/T: max, sum e^(x-m), sum e^(x-m) (x-m)
-    float pad[3];
-};
-
-// merge softmax/entropy partial states (m, s, a)
-__device__ __forceinline__ void merge_msa(float& m, float& s, float& a, float m2, float s2,
-                                          float a2) {
-    if (s2 == 0.f) return;
-    if (s == 0.f) { m = m2; s = s2; a = a2; return; }
-    const float mn = fmaxf(m, m2);
-    const float c1 = expf(m - mn), c2 = expf(m2 - mn);
-    a = c1 * (a + (m - mn) * s) + c2 * (a2 + (m2 - mn) * s2);
-    s = c1 * s + c2 * s2;
-    m = mn;
-}
 
 template <bool TYPICAL>
 __global__ void __launch_bounds__(kStatThreads) row_stats_kernel(const float* __restrict__ logits,
@@ -64,24 +48,7 @@ __global__ void __launch_bounds__(kStatThreads) row_stats_kernel(const float* __
     float m = -INFINITY, s = 0.f, a = 0.f;
     auto take = [&](float l, int v) {
         if (better(l, v, bv, bi)) { bv = l; bi = v; }
-        if (TYPICAL) {
-            const float xv = l * inv_t;
-            if (!(xv > -INFINITY)) return;  // contributes no probability mass
-            if (s == 0.f) {
-                m = xv;
-                s = 1.f;
-                a = 0.f;
-            } else if (xv > m) {
-                const float c1 = expf(m - xv);
-                a = c1 * (a + (m - xv) * s);
-                s = c1 * s + 1.f;
-                m = xv;
-            } else {
-                const float e = expf(xv - m);
-                s += e;
-                a += e * (xv - m);
-            }
-        }
+        if (TYPICAL) take_msa(m, s, a, l * inv_t);
     };
     // vectorised body when the row start is 16-byte aligned
     const bool vec = ((reinterpret_cast<uintptr_t>(x + v0) & 15u) == 0);
@@ -131,54 +98,89 @@ __global__ void __launch_bounds__(kStatThreads) row_stats_kernel(const float* __
     }
 }
 
-constexpr int kAcceptThreads = 512;  // >= max nodes
-
+// One CTA per sequence.  When the statistics kernel flagged a failure (a
+// nonzero a.status entry), every output of the sequence is -1.
 template <bool TYPICAL>
-__global__ void __launch_bounds__(kAcceptThreads) accept_tree_kernel(
-    const float* __restrict__ logits, const int32_t* __restrict__ cand,
-    const int32_t* __restrict__ parent, const int32_t* __restrict__ depth, int N, int V, int Dmax,
-    int nchunk, float inv_t, float eps, float delta, const RowStat* __restrict__ stats,
-    int32_t* __restrict__ accept_len, int32_t* __restrict__ best_node,
-    int32_t* __restrict__ path_nodes, int32_t* __restrict__ next_tok) {
+__global__ void __launch_bounds__(kAcceptThreads) accept_tree_kernel(const AcceptArgs a) {
     __shared__ int s_arg[kAcceptThreads];
-    __shared__ float s_m[kAcceptThreads], s_s[kAcceptThreads], s_tau[kAcceptThreads];
+    __shared__ float s_m[kAcceptThreads], s_s[kAcceptThreads], s_tau[kAcceptThreads],
+        s_cl[kAcceptThreads];
     __shared__ unsigned char s_pass[kAcceptThreads];
     __shared__ int s_best;
     pdl_wait();
     pdl_trigger();
-    const int b = blockIdx.x;
+    const int b = blockIdx.x, N = a.N, V = a.V, Dmax = a.Dmax;
+    const int32_t* parent = a.parent;
+    const int32_t* depth = a.depth;
     const int u = threadIdx.x;
+    int bad = 0;
+    for (int i = u; i < a.nstatus; i += blockDim.x) bad |= a.status[i];
+    if (__syncthreads_or(bad)) {
+        if (u == 0) {
+            a.accept_len[b] = -1;
+            a.best_node[b] = -1;
+            a.next_tok[b] = -1;
+        }
+        for (int e = u; e <= Dmax; e += blockDim.x) a.path_nodes[(size_t)b * (Dmax + 1) + e] = -1;
+        return;
+    }
     if (u < N) {
-        const RowStat* st = stats + ((size_t)b * N + u) * nchunk;
-        float bv = -INFINITY, m = -INFINITY, s = 0.f, a = 0.f;
+        const RowStat* st = a.stats + ((size_t)b * N + u) * a.nchunk;
+        float bv = -INFINITY, m = -INFINITY, s = 0.f, sa = 0.f;
         int bi = INT_MAX;
-        for (int c = 0; c < nchunk; ++c) {
+        for (int c = 0; c < a.nchunk; ++c) {
             const RowStat r = st[c];
             if (better(r.maxv, r.arg, bv, bi)) { bv = r.maxv; bi = r.arg; }
-            if (TYPICAL) merge_msa(m, s, a, r.m, r.s, r.a);
+            if (TYPICAL) merge_msa(m, s, sa, r.m, r.s, r.a);
         }
         s_arg[u] = bi;
         if (TYPICAL) {
             // H = -sum P ln P = ln s - a / s  (x relative to m);  tau = min(eps, delta e^-H)
-            const float H = logf(s) - a / s;
+            const float H = logf(s) - sa / s;
             s_m[u] = m;
             s_s[u] = s;
-            s_tau[u] = fminf(eps, delta * expf(-H));
+            s_tau[u] = fminf(a.eps, a.delta * expf(-H));
         }
     }
     if (threadIdx.x == 0) s_best = 1023;  // node 0 (the root) unless a deeper node wins
+    if (TYPICAL && !a.logits) {
+        // candidate logits from the hidden states: one warp per node, 16-byte loads
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int h8 = a.H / 8;
+        for (int v = 1 + warp; v < N; v += kAcceptThreads / 32) {
+            const int pv = parent[v], tok = a.cand[(size_t)b * N + v];
+            float acc = 0.f;
+            if (pv >= 0 && pv < v && tok >= 0 && tok < V) {
+                const uint4* x = reinterpret_cast<const uint4*>(a.hidden + ((size_t)b * N + pv) * a.H);
+                const uint4* w = reinterpret_cast<const uint4*>(a.lm + (size_t)tok * a.H);
+                for (int c = lane; c < h8; c += 32) {
+                    const uint4 xa = __ldg(x + c), wa = __ldg(w + c);
+                    acc = fmaf(bf16_lo(xa.x), bf16_lo(wa.x), acc);
+                    acc = fmaf(bf16_hi(xa.x), bf16_hi(wa.x), acc);
+                    acc = fmaf(bf16_lo(xa.y), bf16_lo(wa.y), acc);
+                    acc = fmaf(bf16_hi(xa.y), bf16_hi(wa.y), acc);
+                    acc = fmaf(bf16_lo(xa.z), bf16_lo(wa.z), acc);
+                    acc = fmaf(bf16_hi(xa.z), bf16_hi(wa.z), acc);
+                    acc = fmaf(bf16_lo(xa.w), bf16_lo(wa.w), acc);
+                    acc = fmaf(bf16_hi(xa.w), bf16_hi(wa.w), acc);
+                }
+            }
+            acc = warp_sum(acc);
+            if (lane == 0) s_cl[v] = acc;
+        }
+    }
     __syncthreads();
     // candidate tests against the parent's row
     if (u < N) {
         bool pass = true;
         if (u > 0) {
             const int pu = parent[u];
-            const int tok = cand[(size_t)b * N + u];
+            const int tok = a.cand[(size_t)b * N + u];
             if (pu < 0 || pu >= u || tok < 0 || tok >= V) {
                 pass = false;
             } else if (TYPICAL) {
-                const float x = logits[((size_t)b * N + pu) * V + tok] * inv_t;
-                const float P = expf(x - s_m[pu]) / s_s[pu];
+                const float l = a.logits ? a.logits[((size_t)b * N + pu) * V + tok] : s_cl[u];
+                const float P = expf(l * a.inv_t - s_m[pu]) / s_s[pu];
                 pass = P > s_tau[pu];
             } else {
                 pass = tok == s_arg[pu];
@@ -204,10 +206,10 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_tree_kernel(
     if (threadIdx.x == 0) {
         const int best = 1023 - (s_best & 1023);
         const int d = depth[best];
-        accept_len[b] = d;
-        best_node[b] = best;
-        next_tok[b] = s_arg[best];
-        int32_t* path = path_nodes + (size_t)b * (Dmax + 1);
+        a.accept_len[b] = d;
+        a.best_node[b] = best;
+        a.next_tok[b] = s_arg[best];
+        int32_t* path = a.path_nodes + (size_t)b * (Dmax + 1);
         for (int e = 0; e <= Dmax; ++e) path[e] = -1;
         int a_ = best;  // every node on this path passed, so its parents are valid
         while (a_ >= 0) {
@@ -373,6 +375,14 @@ size_t verify_ws(int B, int N, int V) {
 }
 
 }  // namespace
+
+int launch_accept_tree(bool typical, const AcceptArgs& a, cudaStream_t st) {
+    auto k = typical ? accept_tree_kernel<true> : accept_tree_kernel<false>;
+    cudaError_t e = launch(k, dim3(a.B), dim3(kAcceptThreads), 0, st, a);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "accept_tree: launch failed: %s", cudaGetErrorString(e));
+    return MEDUSA_OK;
+}
+
 }  // namespace medusa
 
 using namespace medusa;
@@ -418,12 +428,25 @@ extern "C" int medusa_verify_accept_tree(const float* logits, const int32_t* can
     else
         e = launch(row_stats_kernel<false>, g1, dim3(kStatThreads), 0, st, logits, V, nchunk, inv_t, stats);
     if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "row_stats: launch failed: %s", cudaGetErrorString(e));
-    auto acc = mode == MEDUSA_ACCEPT_TYPICAL ? accept_tree_kernel<true> : accept_tree_kernel<false>;
-    e = launch(acc, dim3(B), dim3(kAcceptThreads), 0, st, logits, cand, parent, depth, N, V, Dmax,
-               nchunk, inv_t, eps, delta, (const RowStat*)stats, accept_len, best_node, path_nodes,
-               next_tok);
-    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "accept_tree: launch failed: %s", cudaGetErrorString(e));
-    return MEDUSA_OK;
+    AcceptArgs aa{};
+    aa.logits = logits;
+    aa.cand = cand;
+    aa.parent = parent;
+    aa.depth = depth;
+    aa.B = B;
+    aa.N = N;
+    aa.V = V;
+    aa.Dmax = Dmax;
+    aa.nchunk = nchunk;
+    aa.inv_t = inv_t;
+    aa.eps = eps;
+    aa.delta = delta;
+    aa.stats = stats;
+    aa.accept_len = accept_len;
+    aa.best_node = best_node;
+    aa.path_nodes = path_nodes;
+    aa.next_tok = next_tok;
+    return launch_accept_tree(mode == MEDUSA_ACCEPT_TYPICAL, aa, st);
 }
 
 extern "C" size_t medusa_verify_chain_workspace(int B, int gamma, int V) {
@@ -447,7 +470,7 @@ extern "C" int medusa_verify_accept_chain(const float* p, const float* q, const 
     ChainPart* parts = reinterpret_cast<ChainPart*>(static_cast<char*>(ws) + plan.off_parts);
     int* firsts = reinterpret_cast<int*>(static_cast<char*>(ws) + plan.off_first);
     cudaStream_t st = as_stream(stream);
-cudaError_t e = launch(chain_scan_kernel, dim3(plan.nchunk, B), dim3(kChainThreads), 0, st, p, q,
+    cudaError_t e = launch(chain_scan_kernel, dim3(plan.nchunk, B), dim3(kChainThreads), 0, st, p, q,
                            draft, gamma, V, plan.nchunk, seed, round, parts, firsts);
     if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "chain_scan: launch failed: %s", cudaGetErrorString(e));
     e = launch(chain_finish_kernel, dim3(B), dim3(32), 0, st, (const ChainPart*)parts,

@@ -104,6 +104,12 @@ def test_host_side_argument_errors(M):
     assert L.medusa_kv_compact(None, None, None, None, None, None, None, None, 1, 1, 1, 128, 10,
                                2, 0, 1, None, None) == -1
     assert L.medusa_build_tree(None, None, None, None, 1, 1, 1, 1, None, None) == -1
+    f0 = C.c_float(0)
+    assert L.medusa_verify_project_tree(None, None, 1, None, None, None, 1, 64, 4096, 32000, 4, 0,
+                                        C.c_float(1), f0, f0, None, None, None, None, None, 0,
+                                        None) == -1
+    assert L.medusa_verify_project_workspace(1, 64, 4100, 32000) == 0   # H % 8 != 0
+    assert L.medusa_verify_project_workspace(1, 513, 4096, 32000) == 0  # N above 512
 
 
 def test_product_path_has_no_cpu_fallback():

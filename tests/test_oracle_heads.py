@@ -77,3 +77,32 @@ def test_topk_k_equals_n_is_a_permutation():
     x = np.array([[3.0, 1.0, 3.0, 2.0]])
     idx, _ = O.topk(x, 4)
     assert idx[0].tolist() == [0, 2, 3, 1]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_lm_head_logits_closed_forms(dtype):
+    # The verifier's next-token logits are lm_head h (Medusa Heads glossary page,
+    # "Tree attention and acceptance": the base model scores each candidate).
+    # Closed forms that a transposed operand or a shifted index would break:
+    #  (1) h = e_j picks column j of lm_head: logits[v] = lm[v, j];
+    #  (2) lm row v = c_v e_{pi(v)} picks one entry of h: logits[v] = c_v h[pi(v)];
+    #  (3) constant h = s and lm = t_v 1: logits[v] = H s t_v.
+    H, V = 24, 37
+    rng = np.random.default_rng(5)
+    lm = (rng.integers(-8, 9, (V, H)) / 4.0).astype(np.float32)  # exact in bf16
+    hs = np.zeros((H, H), np.float32)
+    hs[np.arange(H), np.arange(H)] = 1.0
+    conv = (lambda a: W.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    got = O.lm_head_logits(conv(hs), conv(lm), dtype)                     # [H, V]
+    np.testing.assert_array_equal(got, lm.T.astype(np.float64))
+    pi = rng.permutation(V) % H
+    c = (rng.integers(1, 5, V) / 2.0).astype(np.float32)
+    lm2 = np.zeros((V, H), np.float32)
+    lm2[np.arange(V), pi] = c
+    h2 = (rng.integers(-16, 17, (3, H)) / 8.0).astype(np.float32)
+    got2 = O.lm_head_logits(conv(h2), conv(lm2), dtype)
+    np.testing.assert_array_equal(got2, (h2[:, pi] * c[None]).astype(np.float64))
+    t = (rng.integers(-4, 5, V) / 4.0).astype(np.float32)
+    got3 = O.lm_head_logits(conv(np.full((1, H), 0.5, np.float32)),
+                            conv(np.repeat(t[:, None], H, 1)), dtype)
+    np.testing.assert_array_equal(got3[0], H * 0.5 * t.astype(np.float64))
