@@ -6,8 +6,9 @@
 //
 // The [B*N, V] logits are never written to memory:
 //   project_stats_kernel : CTA (vocab split s, block of 128 rows of the
-//                          flattened [B*N] tree rows).  For each 256-token tile
-//                          of its split, D[128 rows x 256 tokens] = hidden .
+//                          flattened [B*N] tree rows).  For each tile of tn
+//                          tokens (tn in 128..256, chosen so the CTAs of one
+//                          wave get equal work), D[128 rows x tn] = hidden .
 //                          lm_head^T on the tensor cores (tcgen05.mma, bf16 in,
 //                          float32 accumulate in TMEM, two D buffers); TMA
 //                          streams 64-element slices of both operands through
@@ -18,9 +19,10 @@
 //                          warp 0: TMA; warp 1: TMEM allocation and MMA issue;
 //                          warps 2-5: epilogue (warp w reads TMEM lanes
 //                          32*(w%4) .. 32*(w%4)+31)
-//   accept_tree_kernel   : (verify.cu) merges the splits' statistics per row,
-//                          computes the few candidate logits typical
-//                          acceptance needs as dot products, and selects the
+//   row_finish_kernel    : (verify.cu) one warp per row: merges the splits'
+//                          statistics and, for typical acceptance, computes the
+//                          row's candidate logit as a dot product
+//   accept_tree_kernel   : (verify.cu) tests the candidates and selects the
 //                          longest accepted branch.
 // Every wait is bounded; a CTA that gives up marks its status word and the
 // acceptance kernel then writes -1 for every output.
@@ -36,7 +38,7 @@ namespace medusa {
 namespace {
 
 constexpr int kPM = 128;      // tree rows per block (MMA M)
-constexpr int kPN = 256;      // vocab tokens per tile (MMA N)
+constexpr int kPN = 256;      // largest vocab tile (MMA N); the plan picks 128..256
 constexpr int kPK = 64;       // hidden elements per stage (one 128-byte swizzle span)
 constexpr int kPStages = 4;
 constexpr int kPThreads = 192;
@@ -51,7 +53,8 @@ struct ProjArgs {
     int rows;        // B * N
     int V;
     int nkb;         // hidden slices: ceil(H / 64)
-    int tiles;       // ceil(V / 256)
+    int tn;          // vocab tokens per tile, a multiple of 32 in [128, 256]
+    int tiles;       // ceil(V / tn)
     int splits;      // vocab splits (gridDim.x)
     float inv_t;
     RowStat* stats;  // [rows][splits]
@@ -115,15 +118,15 @@ __global__ void __launch_bounds__(kPThreads, 1) project_stats_kernel(
                         break;
                     }
                     const uint32_t sa = sbase + st * kPStage, sb = sa + kPA;
-                    mbar_expect_tx(full(st), kPStage);
+                    mbar_expect_tx(full(st), (uint32_t)(kPA + a.tn * kPK * 2));
                     tma_load_2d(sa, &tma, kb * kPK, nb * kPM, full(st));
-                    tma_load_2d(sb, &tmb, kb * kPK, t * kPN, full(st));
+                    tma_load_2d(sb, &tmb, kb * kPK, t * a.tn, full(st));
                 }
             if (!ok) *fail_flag = 1;
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(kPM, kPN, 0, 0);
+            const uint32_t idesc = idesc_bf16(kPM, a.tn, 0, 0);
             bool ok = true;
             int it = 0;
             for (int tl = 0; tl < ntiles && ok; ++tl) {
@@ -158,33 +161,68 @@ __global__ void __launch_bounds__(kPThreads, 1) project_stats_kernel(
     } else {
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = nb * kPM + q * 32 + lane;
-        float bv = -INFINITY, m = -INFINITY, ssum = 0.f, sa = 0.f;
+        // running argmax (bv, bi) and, for typical acceptance, the softmax state
+        // of x = logit / T in base 2: m2 = max x*log2(e), s = sum 2^(x*log2e - m2),
+        // a2 = sum 2^(..) (x*log2e - m2); a = a2 ln 2 in natural units
+        float bv = -INFINITY, m2 = -INFINITY, ssum = 0.f, sa2 = 0.f;
         int bi = INT_MAX;
+        const float k2 = a.inv_t * 1.4426950408889634f;
         bool ok = true;
         for (int tl = 0; tl < ntiles; ++tl) {
             const int buf = tl & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(d_full(buf), (tl / 2) & 1, kPWait));
             if (!ok) break;
             fence_after_sync();
-            const int v0 = (t0 + tl) * kPN;
+            const int v0 = (t0 + tl) * a.tn;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kPN; c0 += 32) {
+            for (int c0 = 0; c0 < a.tn; c0 += 32) {
                 float x[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPN + c0), x);
                 tmem_wait_ld();
+                const int nv = min(32, a.V - (v0 + c0));  // columns past the vocab are padding
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int v = v0 + c0 + j;
-                    if (v < a.V) {
-                        if (better(x[j], v, bv, bi)) { bv = x[j]; bi = v; }
-                        if (TYPICAL) take_msa(m, ssum, sa, x[j] * a.inv_t);
+                for (int j = 0; j < 32; ++j)
+                    if (j >= nv) x[j] = -INFINITY;
+                // chunk maximum, then its lowest column; a later chunk only wins
+                // with a strictly larger value (its tokens are larger)
+                float cm = x[0];
+#pragma unroll
+                for (int j = 1; j < 32; ++j) cm = fmaxf(cm, x[j]);
+                if (cm > bv) {
+                    int cj = 31;
+#pragma unroll
+                    for (int j = 31; j >= 0; --j)
+                        if (x[j] == cm) cj = j;
+                    bv = cm;
+                    bi = v0 + c0 + cj;
+                }
+                if (TYPICAL && nv > 0) {
+                    const float cm2 = cm * k2;
+                    if (cm2 > m2) {  // move the reference to the chunk maximum
+                        if (ssum > 0.f) {
+                            const float c = umma::exp2_approx(m2 - cm2);
+                            sa2 = c * (sa2 + (m2 - cm2) * ssum);
+                            ssum *= c;
+                        }
+                        m2 = cm2;
                     }
+                    float cs = 0.f, ca = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float d = fmaf(x[j], k2, -m2);  // -inf for padding: e = 0
+                        const float e = umma::exp2_approx(d);
+                        cs += e;
+                        ca = fmaf(e, j < nv ? d : 0.f, ca);
+                    }
+                    ssum += cs;
+                    sa2 += ca;
                 }
             }
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(d_empty(buf));
         }
+        const float m = m2 * 0.6931471805599453f, sa = sa2 * 0.6931471805599453f;
         if (!ok) {
             if (lane == 0) *fail_flag = 1;
         } else if (row < a.rows) {
@@ -231,21 +269,35 @@ int rows_tensor_map(CUtensorMap* m, const void* p, int H, int rows, int box_rows
 }
 
 struct ProjPlan {
-    int rows, nblocks, tiles, splits, nkb;
-    size_t off_status, ws_bytes;
+    int rows, nblocks, tn, tiles, splits, nkb;
+    size_t off_status, off_final, off_cl, ws_bytes;
 };
 
 ProjPlan plan_project(int B, int N, int H, int V) {
     ProjPlan p{};
     p.rows = B * N;
     p.nblocks = (p.rows + kPM - 1) / kPM;
-    p.tiles = (V + kPN - 1) / kPN;
     p.nkb = (H + kPK - 1) / kPK;
-    // one CTA per SM (the operand ring takes most of shared memory)
-    int sp = sm_count() / p.nblocks;
-    p.splits = sp < 1 ? 1 : (sp > p.tiles ? p.tiles : sp);
+    // One CTA per SM (the operand ring takes most of shared memory); each row
+    // block gets `splits` CTAs.  The tile width is the one whose busiest CTA
+    // has the fewest vocab columns (ties: the wider tile).
+    const int per_block = sm_count() / p.nblocks;
+    long long best = -1;
+    for (int tn = kPN; tn >= 128; tn -= 32) {
+        const int tiles = (V + tn - 1) / tn;
+        const int splits = per_block < 1 ? 1 : (per_block > tiles ? tiles : per_block);
+        const long long cols = (long long)((tiles + splits - 1) / splits) * tn;
+        if (best < 0 || cols < best) {
+            best = cols;
+            p.tn = tn;
+            p.tiles = tiles;
+            p.splits = splits;
+        }
+    }
     p.off_status = align_up((size_t)p.rows * p.splits * sizeof(RowStat), 256);
-    p.ws_bytes = align_up(p.off_status + (size_t)p.nblocks * p.splits * sizeof(int), 256);
+    p.off_final = align_up(p.off_status + (size_t)p.nblocks * p.splits * sizeof(int), 256);
+    p.off_cl = align_up(p.off_final + (size_t)p.rows * sizeof(RowStat), 256);
+    p.ws_bytes = align_up(p.off_cl + (size_t)p.rows * sizeof(float), 256);
     return p;
 }
 
@@ -303,13 +355,14 @@ extern "C" int medusa_verify_project_tree(const void* hidden_tree, const void* l
     CUtensorMap tma, tmb;
     rc = rows_tensor_map(&tma, hidden_tree, H, p.rows, kPM);
     if (rc) return rc;
-    rc = rows_tensor_map(&tmb, lm_head, H, V, kPN);
+    rc = rows_tensor_map(&tmb, lm_head, H, V, p.tn);
     if (rc) return rc;
     char* w = static_cast<char*>(ws);
     ProjArgs pa{};
     pa.rows = p.rows;
     pa.V = V;
     pa.nkb = p.nkb;
+    pa.tn = p.tn;
     pa.tiles = p.tiles;
     pa.splits = p.splits;
     pa.inv_t = mode == MEDUSA_ACCEPT_TYPICAL ? 1.f / temperature : 1.f;
@@ -321,11 +374,15 @@ extern "C" int medusa_verify_project_tree(const void* hidden_tree, const void* l
     cudaError_t e = launch(k, dim3(p.splits, p.nblocks), dim3(kPThreads), (size_t)kPSmem, st, tma, tmb, pa);
     if (e != cudaSuccess)
         return fail(MEDUSA_ERR_CUDA, "verify_project_tree: launch failed: %s", cudaGetErrorString(e));
+    RowStat* final_stats = reinterpret_cast<RowStat*>(w + p.off_final);
+    float* child_logit = reinterpret_cast<float*>(w + p.off_cl);
+    rc = launch_row_finish(mode == MEDUSA_ACCEPT_TYPICAL, pa.stats, p.splits, p.rows, N, V, H,
+                           static_cast<const uint16_t*>(hidden_tree), static_cast<const uint16_t*>(lm_head),
+                           cand, parent, final_stats, child_logit, st);
+    if (rc) return rc;
     AcceptArgs aa{};
     aa.logits = nullptr;
-    aa.hidden = static_cast<const uint16_t*>(hidden_tree);
-    aa.lm = static_cast<const uint16_t*>(lm_head);
-    aa.H = H;
+    aa.child_logit = child_logit;
     aa.cand = cand;
     aa.parent = parent;
     aa.depth = depth;
@@ -333,11 +390,11 @@ extern "C" int medusa_verify_project_tree(const void* hidden_tree, const void* l
     aa.N = N;
     aa.V = V;
     aa.Dmax = Dmax;
-    aa.nchunk = p.splits;
+    aa.nchunk = 1;
     aa.inv_t = pa.inv_t;
     aa.eps = eps;
     aa.delta = delta;
-    aa.stats = pa.stats;
+    aa.stats = final_stats;
     aa.status = pa.status;
     aa.nstatus = p.nblocks * p.splits;
     aa.accept_len = accept_len;

@@ -103,8 +103,7 @@ __global__ void __launch_bounds__(kStatThreads) row_stats_kernel(const float* __
 template <bool TYPICAL>
 __global__ void __launch_bounds__(kAcceptThreads) accept_tree_kernel(const AcceptArgs a) {
     __shared__ int s_arg[kAcceptThreads];
-    __shared__ float s_m[kAcceptThreads], s_s[kAcceptThreads], s_tau[kAcceptThreads],
-        s_cl[kAcceptThreads];
+    __shared__ float s_m[kAcceptThreads], s_s[kAcceptThreads], s_tau[kAcceptThreads];
     __shared__ unsigned char s_pass[kAcceptThreads];
     __shared__ int s_best;
     pdl_wait();
@@ -143,32 +142,6 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_tree_kernel(const Accep
         }
     }
     if (threadIdx.x == 0) s_best = 1023;  // node 0 (the root) unless a deeper node wins
-    if (TYPICAL && !a.logits) {
-        // candidate logits from the hidden states: one warp per node, 16-byte loads
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        const int h8 = a.H / 8;
-        for (int v = 1 + warp; v < N; v += kAcceptThreads / 32) {
-            const int pv = parent[v], tok = a.cand[(size_t)b * N + v];
-            float acc = 0.f;
-            if (pv >= 0 && pv < v && tok >= 0 && tok < V) {
-                const uint4* x = reinterpret_cast<const uint4*>(a.hidden + ((size_t)b * N + pv) * a.H);
-                const uint4* w = reinterpret_cast<const uint4*>(a.lm + (size_t)tok * a.H);
-                for (int c = lane; c < h8; c += 32) {
-                    const uint4 xa = __ldg(x + c), wa = __ldg(w + c);
-                    acc = fmaf(bf16_lo(xa.x), bf16_lo(wa.x), acc);
-                    acc = fmaf(bf16_hi(xa.x), bf16_hi(wa.x), acc);
-                    acc = fmaf(bf16_lo(xa.y), bf16_lo(wa.y), acc);
-                    acc = fmaf(bf16_hi(xa.y), bf16_hi(wa.y), acc);
-                    acc = fmaf(bf16_lo(xa.z), bf16_lo(wa.z), acc);
-                    acc = fmaf(bf16_hi(xa.z), bf16_hi(wa.z), acc);
-                    acc = fmaf(bf16_lo(xa.w), bf16_lo(wa.w), acc);
-                    acc = fmaf(bf16_hi(xa.w), bf16_hi(wa.w), acc);
-                }
-            }
-            acc = warp_sum(acc);
-            if (lane == 0) s_cl[v] = acc;
-        }
-    }
     __syncthreads();
     // candidate tests against the parent's row
     if (u < N) {
@@ -179,7 +152,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_tree_kernel(const Accep
             if (pu < 0 || pu >= u || tok < 0 || tok >= V) {
                 pass = false;
             } else if (TYPICAL) {
-                const float l = a.logits ? a.logits[((size_t)b * N + pu) * V + tok] : s_cl[u];
+                const float l = a.logits ? a.logits[((size_t)b * N + pu) * V + tok] : a.child_logit[(size_t)b * N + u];
                 const float P = expf(l * a.inv_t - s_m[pu]) / s_s[pu];
                 pass = P > s_tau[pu];
             } else {
@@ -374,7 +347,107 @@ size_t verify_ws(int B, int N, int V) {
     return align_up((size_t)B * N * nchunk * sizeof(RowStat), 256);
 }
 
+constexpr int kFinishWarps = 8;
+
+// One warp per row: lanes merge the row's split records, then a shuffle tree
+// merges the lanes; for typical acceptance the same warp computes the logit of
+// the row's own candidate against its parent's hidden state.
+template <bool TYPICAL>
+__global__ void __launch_bounds__(kFinishWarps * 32) row_finish_kernel(
+    const RowStat* __restrict__ stats, int splits, int rows, int N, int V, int H,
+    const uint16_t* __restrict__ hidden, const uint16_t* __restrict__ lm,
+    const int32_t* __restrict__ cand, const int32_t* __restrict__ parent, RowStat* __restrict__ out,
+    float* __restrict__ child_logit) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kFinishWarps + (threadIdx.x >> 5);
+    // The dot product runs before the dependency wait: the statistics kernel
+    // (the previous one) writes none of hidden, lm_head or cand, and it lets
+    // this kernel start only after its own wait on everything before it.
+    const int b = row / N, u = row - (row / N) * N;
+    const uint4* x = nullptr;
+    const uint4* w = nullptr;
+    if (TYPICAL && row < rows && u > 0) {
+        const int pu = parent[u], tok = cand[row];
+        if (pu >= 0 && pu < u && tok >= 0 && tok < V) {
+            x = reinterpret_cast<const uint4*>(hidden + ((size_t)b * N + pu) * H);
+            w = reinterpret_cast<const uint4*>(lm + (size_t)tok * H);
+        }
+    }
+    float dot = 0.f;
+    if (x) {
+        constexpr int kU = 4;
+        const int h8 = H / 8;
+        for (int c0 = lane; c0 < h8; c0 += 32 * kU) {
+            uint4 xa[kU], wa[kU];
+#pragma unroll
+            for (int k = 0; k < kU; ++k) {
+                const int c = c0 + 32 * k;
+                xa[k] = c < h8 ? __ldg(x + c) : make_uint4(0, 0, 0, 0);
+                wa[k] = c < h8 ? __ldg(w + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int k = 0; k < kU; ++k) {
+                dot = fmaf(bf16_lo(xa[k].x), bf16_lo(wa[k].x), dot);
+                dot = fmaf(bf16_hi(xa[k].x), bf16_hi(wa[k].x), dot);
+                dot = fmaf(bf16_lo(xa[k].y), bf16_lo(wa[k].y), dot);
+                dot = fmaf(bf16_hi(xa[k].y), bf16_hi(wa[k].y), dot);
+                dot = fmaf(bf16_lo(xa[k].z), bf16_lo(wa[k].z), dot);
+                dot = fmaf(bf16_hi(xa[k].z), bf16_hi(wa[k].z), dot);
+                dot = fmaf(bf16_lo(xa[k].w), bf16_lo(wa[k].w), dot);
+                dot = fmaf(bf16_hi(xa[k].w), bf16_hi(wa[k].w), dot);
+            }
+        }
+        dot = warp_sum(dot);
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (row >= rows) return;
+    if (TYPICAL && lane == 0) child_logit[row] = x ? dot : __int_as_float(0x7fc00000);
+    float bv = -INFINITY, m = -INFINITY, s = 0.f, sa = 0.f;
+    int bi = INT_MAX;
+    const RowStat* st = stats + (size_t)row * splits;
+#pragma unroll 4
+    for (int c = lane; c < splits; c += 32) {
+        const RowStat r = st[c];
+        if (better(r.maxv, r.arg, bv, bi)) { bv = r.maxv; bi = r.arg; }
+        if (TYPICAL) merge_msa(m, s, sa, r.m, r.s, r.a);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        if (TYPICAL) {
+            const float om = __shfl_xor_sync(0xffffffffu, m, o);
+            const float os = __shfl_xor_sync(0xffffffffu, s, o);
+            const float oa = __shfl_xor_sync(0xffffffffu, sa, o);
+            merge_msa(m, s, sa, om, os, oa);
+        }
+    }
+    if (lane == 0) {
+        RowStat r;
+        r.maxv = bv;
+        r.arg = bi;
+        r.m = m;
+        r.s = s;
+        r.a = sa;
+        r.pad[0] = r.pad[1] = r.pad[2] = 0.f;
+        out[row] = r;
+    }
+}
+
 }  // namespace
+
+int launch_row_finish(bool typical, const RowStat* stats, int splits, int rows, int N, int V, int H,
+                      const uint16_t* hidden, const uint16_t* lm, const int32_t* cand,
+                      const int32_t* parent, RowStat* out, float* child_logit, cudaStream_t st) {
+    auto k = typical ? row_finish_kernel<true> : row_finish_kernel<false>;
+    const int grid = (rows + kFinishWarps - 1) / kFinishWarps;
+    cudaError_t e = launch(k, dim3(grid), dim3(kFinishWarps * 32), 0, st, stats, splits, rows, N, V, H,
+                           hidden, lm, cand, parent, out, child_logit);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "row_finish: launch failed: %s", cudaGetErrorString(e));
+    return MEDUSA_OK;
+}
 
 int launch_accept_tree(bool typical, const AcceptArgs& a, cudaStream_t st) {
     auto k = typical ? accept_tree_kernel<true> : accept_tree_kernel<false>;

@@ -47,13 +47,11 @@ __device__ __forceinline__ void take_msa(float& m, float& s, float& a, float xv)
 }
 
 // Arguments of the acceptance kernel.  The candidate logit of node u (row
-// parent(u), token cand[u]) is read from `logits` when given, else computed as
-// hidden[b, parent(u)] . lm[cand[u]] (bf16 rows of H elements, float32 sum).
+// parent(u), token cand[u]) is read from `logits` when given, else from
+// child_logit[b*N + u].
 struct AcceptArgs {
-    const float* logits;      // [B,N,V] or nullptr
-    const uint16_t* hidden;   // [B,N,H] bf16 (when logits is nullptr)
-    const uint16_t* lm;       // [V,H] bf16
-    int H;
+    const float* logits;       // [B,N,V] or nullptr
+    const float* child_logit;  // [B*N] (when logits is nullptr)
     const int32_t* cand;
     const int32_t* parent;
     const int32_t* depth;
@@ -69,5 +67,13 @@ struct AcceptArgs {
 };
 constexpr int kAcceptThreads = 512;  // >= max nodes
 int launch_accept_tree(bool typical, const AcceptArgs& a, cudaStream_t st);
+
+// Per-row finish of the fused projection's statistics: merges the `splits`
+// records of each of the `rows` rows into out[row] and, for typical
+// acceptance, writes child_logit[b*N + u] = hidden[b, parent(u)] . lm[cand[b,u]]
+// (bf16 rows of H elements, float32 sum; NaN where parent or token is invalid).
+int launch_row_finish(bool typical, const RowStat* stats, int splits, int rows, int N, int V, int H,
+                      const uint16_t* hidden, const uint16_t* lm, const int32_t* cand,
+                      const int32_t* parent, RowStat* out, float* child_logit, cudaStream_t st);
 
 }  // namespace medusa
