@@ -12,6 +12,11 @@ with every input resident in HBM.  The step reads ~1.52 GB, more than L2, so
 consecutive steps start cold.  kv_len is restored before each step (compaction
 grows it) so every step sees the same workload.
 
+Beside the step, the JSON line carries "verify_projection": the fused
+verification projection (lm_head x tree hidden states on the tensor cores,
+reduced to acceptance without writing logits) timed at the step's shapes and at
+batch 4 of the dense 341-node tree.
+
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
 bounded sample of the same step instead.
 """
@@ -43,7 +48,7 @@ WORKLOAD = ("vicuna7b-shaped medusa step, batch 1: hidden 4096, vocab 32000, 5 h
 # DRAM bytes per launch of the heads call, from the ncu capture summarised in
 # profiles/ (dram__bytes_read.sum + dram__bytes_write.sum summed over its three
 # kernels), with the sha1 of heads.cu it was taken on; null once that file changes.
-HEADS_TRAFFIC = {"sha1": None, "bytes": None}
+HEADS_TRAFFIC = {"sha1": "3f0b467a704b63b419fb7cc805600417ab27a526", "bytes": 1479551933}
 
 
 def _sha1(path):
@@ -58,6 +63,14 @@ def _peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def _tpeak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def _tree_tables():
@@ -267,6 +280,64 @@ def run_e2e(step, steps, warmup):
     return dt, h2d, d2h
 
 
+def measure_projection(dev, iters=50, warmup=5):
+    """medusa_verify_project_tree (lm_head x tree hidden states on the tensor
+    cores, reduced to acceptance without writing logits) at two shapes: the
+    Vicuna-7B-shaped batch-1 sparse tree (greedy; HBM-bound: lm_head is read
+    once) and batch 4 of the dense 341-node tree (typical; tensor-bound).
+    Each is timed over `iters` back-to-back calls with events at both ends."""
+    import torch
+    import medusa_speculative_decoding_gb300 as M
+    c = CFG
+    H, V = c["H"], c["V"]
+    td = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    lm = td(W.normal(2, "LMHEAD", (V, H), 0.02, "bf16"))
+    dense_paths = np.array([[a, b, x, y] for a in range(4) for b in range(4) for x in range(4)
+                            for y in range(4)], np.int32)
+    cases = (("vicuna7b_b1_sparse64_greedy", M.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5, 1, 5, 8,
+              "greedy", "hbm"),
+             ("dense341_b4_typical", dense_paths, 4, 4, 4, 4, "typical", "tensor"))
+    out = {}
+    for name, paths, maxd, B, K, k, mode, bound in cases:
+        t = M.tree_layout(paths, maxd)
+        N = t["N"]
+        hid = td(W.hidden_tree(4, B, N, H, "bf16"))
+        par, dep, rnk = (torch.from_numpy(t[x]).to(dev) for x in ("parent", "depth", "rank"))
+        lists = torch.from_numpy(W.random_topk_lists(4, B, K, k, V)).to(dev)
+        cand = M.build_tree(lists, torch.from_numpy(W.root_tokens(4, B, V)).to(dev), dep, rnk)
+        ws = torch.empty(max(16, M.verify_project_workspace(B, N, H, V)), dtype=torch.uint8, device=dev)
+        res = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   best_node=torch.empty(B, dtype=torch.int32, device=dev),
+                   path_nodes=torch.empty((B, t["max_depth"] + 1), dtype=torch.int32, device=dev),
+                   next_tok=torch.empty(B, dtype=torch.int32, device=dev))
+        call = lambda: M.verify_project_tree(hid, lm, cand, par, dep, t["max_depth"], mode, out=res, ws=ws)
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            call()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / iters
+        rows = B * N
+        if bound == "hbm":
+            by = V * H * 2 + rows * H * 2
+            peak, kind = _peaks()
+            ach = by / (us * 1e-6) / 1e9
+            out[name] = {"us": us, "bound": "hbm", "achieved": ach, "unit": "GB/s", "peak": peak,
+                         "peak_kind": kind, "frac": ach / peak, "algorithmic_bytes": by, "rows": rows}
+        else:
+            fl = 2.0 * rows * V * H
+            peak, kind = _tpeak()
+            ach = fl / (us * 1e-6) / 1e12
+            out[name] = {"us": us, "bound": "tensor", "achieved": ach, "unit": "TFLOP/s", "peak": peak,
+                         "peak_kind": kind, "frac": ach / peak, "algorithmic_flops": fl, "rows": rows}
+        del hid, ws
+    return out
+
+
 # ----------------------------------------------------------------------------
 # oracle timing (CPU baseline and the reference arm)
 # ----------------------------------------------------------------------------
@@ -428,6 +499,8 @@ def main():
     e2e_s, h2d, d2h = run_e2e(step, max(20, K // 4), args.warmup)
     e2e_val = world * max(20, K // 4) / e2e_s
 
+    proj = measure_projection(dev) if world == 1 or rank == 0 else None
+
     peak, peak_kind = _peaks()
     hb, ab, vb = algorithmic_bytes(c, N, int(inp["kv_len"][0]) + N)
     heads_gbs = hb / (heads_ms * 1e-3) / 1e9
@@ -449,6 +522,7 @@ def main():
             "attention": {"achieved": att_gbs, "unit": "GB/s", "frac": att_gbs / peak,
                           "algorithmic_bytes": ab, "ms": att_ms},
             "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
+            "verify_projection": proj,
             "clocks": clocks,
             "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
