@@ -44,13 +44,26 @@ __device__ __forceinline__ float load_scalar<uint16_t>(const uint16_t* p, size_t
     return bf16_to_f32(p[i]);
 }
 
-// acc += dot(16-byte weight chunk, x[0..n))
+// Shared-memory layout of one float32 vector of H elements.  float32 weights:
+// plain.  bf16 weights (16-byte chunks of 8 elements): elements 0-3 of chunk c
+// sit at 4c and elements 4-7 at H/2 + 4c, so the lanes of a warp, which read
+// consecutive chunks, read consecutive 16-byte words of each half (no bank
+// conflicts).
 template <typename WT>
-__device__ __forceinline__ float dot_chunk(const uint4& w, const float* x, float acc);
+__device__ __forceinline__ int xpos(int i, int H) {
+    if (sizeof(WT) == 4) return i;
+    return ((i >> 2) & 1) * (H >> 1) + ((i >> 3) << 2) + (i & 3);
+}
+
+// acc += dot(16-byte weight chunk c, x[chunk c]); xlo / xhi point at the
+// chunk's two float4 halves (xhi unused for float32 weights)
+template <typename WT>
+__device__ __forceinline__ float dot_chunk(const uint4& w, const float* xlo, const float* xhi, float acc);
 template <>
-__device__ __forceinline__ float dot_chunk<uint16_t>(const uint4& w, const float* x, float acc) {
-    const float4 a = *reinterpret_cast<const float4*>(x);
-    const float4 b = *reinterpret_cast<const float4*>(x + 4);
+__device__ __forceinline__ float dot_chunk<uint16_t>(const uint4& w, const float* xlo, const float* xhi,
+                                                     float acc) {
+    const float4 a = *reinterpret_cast<const float4*>(xlo);
+    const float4 b = *reinterpret_cast<const float4*>(xhi);
     acc = fmaf(bf16_lo(w.x), a.x, acc);
     acc = fmaf(bf16_hi(w.x), a.y, acc);
     acc = fmaf(bf16_lo(w.y), a.z, acc);
@@ -62,8 +75,8 @@ __device__ __forceinline__ float dot_chunk<uint16_t>(const uint4& w, const float
     return acc;
 }
 template <>
-__device__ __forceinline__ float dot_chunk<float>(const uint4& w, const float* x, float acc) {
-    const float4 a = *reinterpret_cast<const float4*>(x);
+__device__ __forceinline__ float dot_chunk<float>(const uint4& w, const float* xlo, const float*, float acc) {
+    const float4 a = *reinterpret_cast<const float4*>(xlo);
     acc = fmaf(__uint_as_float(w.x), a.x, acc);
     acc = fmaf(__uint_as_float(w.y), a.y, acc);
     acc = fmaf(__uint_as_float(w.z), a.z, acc);
@@ -72,8 +85,9 @@ __device__ __forceinline__ float dot_chunk<float>(const uint4& w, const float* x
 }
 
 // Partial dot products of rows row0..row0+R-1 of W ([rows][H]) with the NB
-// shared-memory vectors xs[b*H ..].  Rows past last_row repeat last_row (their
-// results are discarded by the caller).  Each lane covers chunks lane, lane+32..
+// shared-memory vectors xs[b*H ..] (laid out as xpos says).  Rows past
+// last_row repeat last_row (their results are discarded by the caller).  Each
+// lane covers chunks lane, lane+32..
 template <typename WT, int NB, int R, int U>
 __device__ __forceinline__ void dot_rows(const WT* __restrict__ W, int row0, int last_row, int H,
                                          const float* __restrict__ xs, float (&acc)[R][NB],
@@ -101,43 +115,54 @@ __device__ __forceinline__ void dot_rows(const WT* __restrict__ W, int row0, int
         for (int u = 0; u < U; ++u) {
             const int c = c0 + 32 * u;
             if (c < nchunk) {
-                const float* xc = xs + (size_t)c * VEC;
+                const float* xlo = xs + (size_t)c * 4;  // see xpos
+                const float* xhi = xlo + (H >> 1);
 #pragma unroll
                 for (int b = 0; b < NB; ++b)
 #pragma unroll
                     for (int r = 0; r < R; ++r)
-                        acc[r][b] = dot_chunk<WT>(w[u][r], xc + (size_t)b * H, acc[r][b]);
+                        acc[r][b] = dot_chunk<WT>(w[u][r], xlo + (size_t)b * H, xhi + (size_t)b * H, acc[r][b]);
             }
         }
     }
 }
 
-// dst[0..8) = the eight bf16 values of w, or dst[0..4) = the four floats of w
+// Chunk c (16 bytes) of a vector into its shared-memory places (see xpos); xv
+// is the vector's base in shared memory.
 template <typename WT>
-__device__ __forceinline__ void store_chunk(const uint4& w, float* dst);
+__device__ __forceinline__ void store_chunk(const uint4& w, float* xv, int c, int H);
 template <>
-__device__ __forceinline__ void store_chunk<uint16_t>(const uint4& w, float* dst) {
-    reinterpret_cast<float4*>(dst)[0] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
-    reinterpret_cast<float4*>(dst)[1] = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+__device__ __forceinline__ void store_chunk<uint16_t>(const uint4& w, float* xv, int c, int H) {
+    *reinterpret_cast<float4*>(xv + 4 * c) = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+    *reinterpret_cast<float4*>(xv + (H >> 1) + 4 * c) =
+        make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
 }
 template <>
-__device__ __forceinline__ void store_chunk<float>(const uint4& w, float* dst) {
-    *reinterpret_cast<float4*>(dst) =
+__device__ __forceinline__ void store_chunk<float>(const uint4& w, float* xv, int c, int) {
+    *reinterpret_cast<float4*>(xv + 4 * c) =
         make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w));
 }
 
-// dst[0..n) = src[0..n) as float32, with 16-byte loads when src is aligned
-// (n is a multiple of 8, dst 16-byte aligned).  The loads are cached in L2 only:
-// src may have been written by the previous kernel on the stream.
+// The NB vectors src[b*H .. b*H + H) as float32 into dst[b*H ..] (xpos
+// layout), with 16-byte loads when src is aligned (H is a multiple of 8, dst
+// 16-byte aligned).  The loads are cached in L2 only: src may have been
+// written by the previous kernel on the stream.
 template <typename WT>
-__device__ __forceinline__ void load_vector_to_smem(const WT* src, float* dst, int n) {
+__device__ __forceinline__ void load_vector_to_smem(const WT* src, float* dst, int NB, int H) {
     constexpr int VEC = Elems<WT>::n;
     if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
         const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        const int per = H / VEC;
 #pragma unroll 4
-        for (int c = threadIdx.x; c < n / VEC; c += blockDim.x) store_chunk<WT>(__ldcg(s4 + c), dst + c * VEC);
+        for (int c = threadIdx.x; c < NB * per; c += blockDim.x) {
+            const int b = c / per;
+            store_chunk<WT>(__ldcg(s4 + c), dst + (size_t)b * H, c - b * per, H);
+        }
     } else {
-        for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = load_scalar<WT>(src, i);
+        for (int i = threadIdx.x; i < NB * H; i += blockDim.x) {
+            const int b = i / H, j = i - b * H;
+            dst[(size_t)b * H + xpos<WT>(j, H)] = load_scalar<WT>(src, i);
+        }
     }
 }
 
@@ -154,7 +179,7 @@ __global__ void __launch_bounds__(THREADS) heads_w1_silu_kernel(
     pdl_wait();  // h may come from the previous kernel (the last round's compaction)
     if (blockIdx.x == 0)
         for (int k = threadIdx.x; k < K; k += THREADS) done[k] = 0u;
-    load_vector_to_smem<WT>(h, xs, NB * H);
+    load_vector_to_smem<WT>(h, xs, NB, H);
     __syncthreads();
     pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -176,7 +201,7 @@ __global__ void __launch_bounds__(THREADS) heads_w1_silu_kernel(
                     const int i = i0 + r;
                     const float u = s + load_scalar<WT>(b1, (size_t)k * H + i);
                     const float silu = u / (1.f + expf(-u));
-                    z[((size_t)b * K + k) * H + i] = xs[(size_t)b * H + i] + silu;
+                    z[((size_t)b * K + k) * H + i] = xs[(size_t)b * H + xpos<WT>(i, H)] + silu;
                 }
             }
     }
@@ -235,12 +260,14 @@ __global__ void __launch_bounds__(THREADS) heads_w2_topk_kernel(
     }
     pdl_wait();
     {
-        // z rows are 16-byte aligned (H % 8 == 0); L2-only loads, K1 wrote them
+        // z rows are 16-byte aligned (H % 8 == 0); L2-only loads, K1 wrote them.
+        // float4 j holds elements 4j..4j+3 (xpos layout: half j & 1 of chunk j / 2)
         const int h4 = H / 4;
 #pragma unroll 4
         for (int c = threadIdx.x; c < NB * h4; c += THREADS) {
             const int b = c / h4, j = c - b * h4;
-            reinterpret_cast<float4*>(xs)[c] =
+            const int dst = sizeof(WT) == 4 ? 4 * j : (j & 1) * (H >> 1) + 4 * (j >> 1);
+            *reinterpret_cast<float4*>(xs + (size_t)b * H + dst) =
                 __ldcg(reinterpret_cast<const float4*>(z + ((size_t)b * K + k) * H) + j);
         }
     }
