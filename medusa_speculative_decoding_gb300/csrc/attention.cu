@@ -141,12 +141,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
 
     const int split = blockIdx.x, S = gridDim.x;
     const int hk = blockIdx.y / a.qblocks, qb = blockIdx.y % a.qblocks;
-    const int b = blockIdx.z;
     const int N = a.N, G = a.G;
-    if (threadIdx.x == kTmaWarp * 32) {
+    if (threadIdx.x == kTmaWarp * 32 && a.B == 1) {
         // Warm L2 with this split's first K and V tiles while the previous kernel
         // finishes.  The rows come from the split's nominal range (no input is
         // read before the dependency wait); a prefetch is only a hint.
+        const int b = 0;
         const size_t head = ((size_t)b * a.Hkv + hk) * a.Lmax;
         for (int t = 0; t < kRing; ++t) {
             const int key0 = split * a.chunk + t * kBlockN;
@@ -158,6 +158,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
     }
     pdl_wait();
     pdl_trigger();
+    // Sequences are taken longest first: blockIdx.z is a rank in the order of
+    // decreasing KV length (ties by index), so the CTAs launched first carry
+    // the most work and the short sequences fill the tail of the grid.
+    __shared__ int s_seq;
+    int b = blockIdx.z;
+    if (a.B > 1 && a.B <= kAttnThreads) {
+        const int t = threadIdx.x;
+        if (t < a.B) {
+            const int Lt = clamp_len(a.kv_len[t], N, a.Lmax);
+            int rank = 0;
+            for (int j = 0; j < a.B; ++j) {
+                const int Lj = clamp_len(a.kv_len[j], N, a.Lmax);
+                rank += (Lj > Lt || (Lj == Lt && j < t)) ? 1 : 0;
+            }
+            if (rank == (int)blockIdx.z) s_seq = t;
+        }
+        __syncthreads();
+        b = s_seq;
+    }
     const int Lb = clamp_len(a.kv_len[b], N, a.Lmax);
     const int total = Lb + N;
     const int k_begin = split * a.chunk;
@@ -601,14 +620,22 @@ AttnPlan plan_attention(int B, int N, int Hq, int Hkv, int D, int Lmax) {
     const long long units = (long long)B * Hkv * p.qblocks;
     const long long target = (long long)sm_count();
     const int max_tiles = (Lmax + kBlockN - 1) / kBlockN;
-    // cost in tile times: each wave takes the CTA's set-up (about kSetupTiles
-    // tiles: TMEM, barriers, Q, pipeline fill) plus its tiles
+    // cost in tile times: a CTA takes its set-up (about kSetupTiles tiles:
+    // TMEM, barriers, Q, pipeline fill) plus its tiles.  With fewer units than SMs every wave runs CTAs of one size; with
+    // at least as many units as SMs (batches, taken longest first) the CTAs
+    // pack the SMs, so the cost is the larger of one CTA and an even share.
     constexpr int kSetupTiles = 4;
     int best = 1;
     long long best_cost = -1;
     for (int s = 1; s <= max_tiles && s <= kMaxSplits; ++s) {
-        const long long waves = (units * s + target - 1) / target;
-        const long long cost = waves * (kSetupTiles + (max_tiles + s - 1) / s);
+        const long long per_cta = kSetupTiles + (max_tiles + s - 1) / s;
+        long long cost;
+        if (B > 1 && units >= target) {
+            const long long share = (units * s * per_cta + target - 1) / target;
+            cost = share > per_cta ? share : per_cta;
+        } else {
+            cost = (units * s + target - 1) / target * per_cta;
+        }
         if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = s; }
     }
     int chunk = (Lmax + best - 1) / best;
