@@ -12,7 +12,8 @@ with every input resident in HBM.  The step reads ~1.52 GB, more than L2, so
 consecutive steps start cold.  kv_len is restored before each step (compaction
 grows it) so every step sees the same workload.
 
-Beside the step, the JSON line carries "verify_projection": the fused
+Beside the step, the JSON line carries "attention_workloads" (tree attention
+alone at the batch-8 ragged and batch-4 KV-8192 shapes) and "verify_projection": the fused
 verification projection (lm_head x tree hidden states on the tensor cores,
 reduced to acceptance without writing logits) timed at the step's shapes and at
 batch 4 of the dense 341-node tree.
@@ -338,6 +339,59 @@ def measure_projection(dev, iters=50, warmup=5):
     return out
 
 
+def measure_attention_workloads(dev, iters=20, warmup=3):
+    """medusa_tree_attention alone at the other workloads' shapes: batch 8 of
+    the 13B shape (40 heads, ragged KV lengths 1024..4096, sparse tree) and
+    batch 4 at KV 8192 with the sparse 64-node and the dense 341-node trees.
+    Each is timed over `iters` back-to-back calls with events at both ends (the
+    KV cache of each exceeds L2)."""
+    import torch
+    import medusa_speculative_decoding_gb300 as M
+    dense_paths = np.array([[a, b, x, y] for a in range(4) for b in range(4) for x in range(4)
+                            for y in range(4)], np.int32)
+    cases = (("13b_b8_ragged_sparse64", M.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5, 8, 40,
+              W.kv_lengths(3, 8, 1024, 4096)),
+             ("b4_kv8192_sparse64", M.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5, 4, 32,
+              np.full(4, 8192, np.int32)),
+             ("b4_kv8192_dense341", dense_paths, 4, 4, 32, np.full(4, 8192, np.int32)))
+    hbm, _ = _peaks()
+    tpk, _ = _tpeak()
+    D = 128
+    out = {}
+    for name, paths, maxd, B, Hq, lens in cases:
+        t = M.tree_layout(paths, maxd)
+        N = t["N"]
+        Lmax = int(lens.max()) + N
+        g = torch.Generator(device=dev)
+        g.manual_seed(7)
+        q = torch.randn(B, N, Hq, D, device=dev, generator=g).bfloat16()
+        kc = torch.randn(B, Hq, Lmax, D, device=dev, generator=g).bfloat16()
+        vc = torch.randn(B, Hq, Lmax, D, device=dev, generator=g).bfloat16()
+        kl = torch.from_numpy(lens.astype(np.int32)).to(dev)
+        mask = torch.from_numpy(t["mask"].view(np.int64)).to(dev)
+        o = torch.empty(B, N, Hq, D, device=dev)
+        ws = torch.empty(max(16, M.tree_attention_workspace(B, N, Hq, Hq, D, Lmax)), dtype=torch.uint8,
+                         device=dev)
+        call = lambda: M.tree_attention(q, kc, vc, kl, mask, out=o, ws=ws)
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            call()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / iters
+        by = sum(2 * Hq * (int(L) + N) * D * 2 for L in lens) + B * N * Hq * D * (2 + 4)
+        fl = sum(4.0 * N * Hq * D * (int(L) + N) for L in lens)
+        out[name] = {"us": us, "gbs": by / (us * 1e-6) / 1e9, "frac_hbm": by / (us * 1e-6) / 1e9 / hbm,
+                     "tflops": fl / (us * 1e-6) / 1e12, "frac_bf16": fl / (us * 1e-6) / 1e12 / tpk,
+                     "algorithmic_bytes": by, "flops_upper_bound": fl}
+        del q, kc, vc, o
+    return out
+
+
 # ----------------------------------------------------------------------------
 # oracle timing (CPU baseline and the reference arm)
 # ----------------------------------------------------------------------------
@@ -399,6 +453,24 @@ def cpu_baseline(inp):
 
 
 # ----------------------------------------------------------------------------
+# replicas: every rank runs its own batch; the job's time is the slowest rank's
+def max_over_ranks(ms, world, device):
+    """The largest of the ranks' timed-region milliseconds (ms itself at world 1)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(steps, ms_total, world):
+    """Whole-job steps/s: every one of `world` replicas ran `steps` steps within
+    the slowest rank's `ms_total` milliseconds."""
+    return world * steps / (ms_total / 1e3)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -484,22 +556,19 @@ def main():
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms_total = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(start.elapsed_time(end), world, dev)
     call_ms = {name: statistics.mean(evs[i][c].elapsed_time(evs[i][c + 1]) for i in range(K))
                for c, name in enumerate(Step.CALLS)}
     heads_ms = call_ms["heads_topk"]
     att_ms = call_ms["tree_attention"]
     ms_step = ms_total / K
-    value = world * K / (ms_total / 1e3)
+    value = replica_throughput(K, ms_total, world)
 
     e2e_s, h2d, d2h = run_e2e(step, max(20, K // 4), args.warmup)
     e2e_val = world * max(20, K // 4) / e2e_s
 
     proj = measure_projection(dev) if world == 1 or rank == 0 else None
+    att_w = measure_attention_workloads(dev) if world == 1 or rank == 0 else None
 
     peak, peak_kind = _peaks()
     hb, ab, vb = algorithmic_bytes(c, N, int(inp["kv_len"][0]) + N)
@@ -523,6 +592,7 @@ def main():
                           "algorithmic_bytes": ab, "ms": att_ms},
             "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
             "verify_projection": proj,
+            "attention_workloads": att_w,
             "clocks": clocks,
             "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
