@@ -13,7 +13,9 @@ consecutive steps start cold.  kv_len is restored before each step (compaction
 grows it) so every step sees the same workload.
 
 Beside the step, the JSON line carries "attention_workloads" (tree attention
-alone at the batch-8 ragged and batch-4 KV-8192 shapes) and "verify_projection": the fused
+alone at the batch-8 ragged and batch-4 KV-8192 shapes), "chain_acceptance"
+(speculative-sampling acceptance at batch 64, vocab 128256) and
+"verify_projection": the fused
 verification projection (lm_head x tree hidden states on the tensor cores,
 reduced to acceptance without writing logits) timed at the step's shapes and at
 batch 4 of the dense 341-node tree.
@@ -392,6 +394,51 @@ def measure_attention_workloads(dev, iters=20, warmup=3):
     return out
 
 
+def measure_chain(dev, gammas=(1, 4, 8, 32), sigma=0.5, reps=10):
+    """medusa_verify_accept_chain at batch 64, vocab 128256 (the speculative-
+    sampling sweep's shape): q = softmax(ql), p = softmax(ql + N(0, sigma)),
+    ql ~ N(0, 2), drafts drawn from q; L2 is flushed (a 512 MB write) before
+    every timed call, and each call is timed alone with events.  Algorithmic
+    bytes: the gathered p and q entries of the drafts examined, plus the row the
+    draw reads (p and q at a rejection, 8V bytes; p alone for a bonus, 4V)."""
+    import torch
+    import medusa_speculative_decoding_gb300 as M
+    B, V = 64, 128256
+    hbm, _ = _peaks()
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    for gamma in gammas:
+        ql = torch.randn(B, gamma + 1, V, device=dev, generator=g) * 2.0
+        p = torch.softmax(ql + sigma * torch.randn(B, gamma + 1, V, device=dev, generator=g), -1)
+        q = torch.softmax(ql[:, :gamma], -1).contiguous()
+        draft = torch.multinomial(q.reshape(-1, V), 1, generator=g).reshape(B, gamma).to(torch.int32)
+        del ql
+        ws = torch.empty(max(16, M.verify_chain_workspace(B, gamma, V)), dtype=torch.uint8, device=dev)
+        n_acc = torch.empty(B, dtype=torch.int32, device=dev)
+        toks = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
+        ts, by = [], []
+        for r in range(reps + 2):
+            flush.fill_(r & 255)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            M.verify_accept_chain(p, q, draft, 1234, r, out=(n_acc, toks), ws=ws)
+            b.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                ts.append(a.elapsed_time(b) * 1e3)
+                na = n_acc.cpu().numpy()
+                by.append(int(sum((8 * (int(n) + 1) + (4 * V if n == gamma else 8 * V)) for n in na)))
+        us = statistics.median(ts)
+        bb = statistics.mean(by)
+        out[f"gamma{gamma}"] = {"us": us, "algorithmic_bytes": bb, "gbs": bb / (us * 1e-6) / 1e9,
+                                "frac_hbm": bb / (us * 1e-6) / 1e9 / hbm}
+        del p, q, draft, ws
+    del flush
+    return out
+
+
 # ----------------------------------------------------------------------------
 # oracle timing (CPU baseline and the reference arm)
 # ----------------------------------------------------------------------------
@@ -569,6 +616,7 @@ def main():
 
     proj = measure_projection(dev) if world == 1 or rank == 0 else None
     att_w = measure_attention_workloads(dev) if world == 1 or rank == 0 else None
+    chain = measure_chain(dev) if world == 1 or rank == 0 else None
 
     peak, peak_kind = _peaks()
     hb, ab, vb = algorithmic_bytes(c, N, int(inp["kv_len"][0]) + N)
@@ -593,6 +641,7 @@ def main():
             "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
             "verify_projection": proj,
             "attention_workloads": att_w,
+            "chain_acceptance": chain,
             "clocks": clocks,
             "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

@@ -196,12 +196,15 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_tree_kernel(const Accep
 // ---------------------------------------------------------------------------
 // SplitMix64 (Steele, Lea and Flood, 2014)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t sm64(uint64_t state, uint64_t n) {
-    uint64_t z = state + n * 0x9E3779B97F4A7C15ull;
+constexpr uint64_t kSmGamma = 0x9E3779B97F4A7C15ull;
+// the output function applied to the advanced state
+__device__ __forceinline__ uint64_t sm_mix(uint64_t z) {
     z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
     z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
     return z ^ (z >> 31);
 }
+// n-th output from state: the state advanced n times by the constant, mixed
+__device__ __forceinline__ uint64_t sm64(uint64_t state, uint64_t n) { return sm_mix(state + n * kSmGamma); }
 __device__ __forceinline__ uint64_t row_key(uint64_t seed, uint64_t stream, uint64_t b,
                                             uint64_t round, uint64_t pos) {
     uint64_t x = sm64(seed, 1);
@@ -216,7 +219,7 @@ __device__ __forceinline__ float u24p(uint64_t h) {
 }
 
 constexpr int kChainThreads = 256;
-constexpr int kChainChunk = 8192;
+constexpr int kChainChunk = 4096;
 
 struct ChainPart {  // per (sequence, chunk)
     float key;      // best race key
@@ -262,39 +265,84 @@ __global__ void __launch_bounds__(kChainThreads) chain_scan_kernel(
     const float* qr = bonus ? nullptr : q + ((size_t)b * gamma + (pos - 1)) * V;
     const uint64_t key = row_key(seed, bonus ? 3 : 2, b, round, pos);
     const int v0 = c * kChainChunk, v1 = min(V, v0 + kChainChunk);
-    float bk = INFINITY, pm = -INFINITY;
-    int bt = INT_MAX, pi = INT_MAX;
-    for (int v = v0 + threadIdx.x; v < v1; v += kChainThreads) {
-        const float pv = pr[v];
-        if (better(pv, v, pm, pi)) { pm = pv; pi = v; }
-        const float w = bonus ? pv : pv - qr[v];
+    // The thread's best race key is kept as the fraction be / bw (E = -ln U+,
+    // w the weight) and compared by cross-multiplication (one division per
+    // thread, not per element).  The largest p is tracked without its index:
+    // the index is looked up afterwards, only when no weight is positive.
+    float be = INFINITY, bw = 1.f, pm = -INFINITY;
+    int bt = INT_MAX;
+    auto take = [&](float pv, float qv, int v, uint64_t z) {  // z = key + (v + 1) * gamma
+        pm = fmaxf(pm, pv);
+        const float w = bonus ? pv : pv - qv;
         if (w > 0.f) {
-            const float k = -logf(u24p(sm64(key, (uint64_t)v + 1))) / w;
-            if (k < bk || (k == bk && v < bt)) { bk = k; bt = v; }
+            const float e = -logf(u24p(sm_mix(z)));
+            const float lhs = e * bw, rhs = be * w;
+            if (lhs < rhs || (lhs == rhs && v < bt)) { be = e; bw = w; bt = v; }
         }
+    };
+    const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0 &&
+                     (bonus || (reinterpret_cast<uintptr_t>(q) & 15u) == 0);
+    if (vec) {
+        // every 16-byte load of the chunk is issued before any element is used
+        constexpr int kPer = kChainChunk / (4 * kChainThreads);
+        uint4 pw[kPer], qw[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int v = v0 + 4 * (threadIdx.x + kChainThreads * k);
+            pw[k] = v < v1 ? ld_stream16(pr + v) : make_uint4(0, 0, 0, 0);
+            qw[k] = (v < v1 && !bonus) ? ld_stream16(qr + v) : make_uint4(0, 0, 0, 0);
+        }
+        const uint64_t zstep = (uint64_t)(4 * kChainThreads) * kSmGamma;
+        uint64_t z = key + (uint64_t)(v0 + 4 * threadIdx.x + 1) * kSmGamma;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k, z += zstep) {
+            const int v = v0 + 4 * (threadIdx.x + kChainThreads * k);
+            if (v < v1) {
+                take(__uint_as_float(pw[k].x), __uint_as_float(qw[k].x), v, z);
+                take(__uint_as_float(pw[k].y), __uint_as_float(qw[k].y), v + 1, z + kSmGamma);
+                take(__uint_as_float(pw[k].z), __uint_as_float(qw[k].z), v + 2, z + 2 * kSmGamma);
+                take(__uint_as_float(pw[k].w), __uint_as_float(qw[k].w), v + 3, z + 3 * kSmGamma);
+            }
+        }
+    } else {
+        for (int v = v0 + threadIdx.x; v < v1; v += kChainThreads)
+            take(pr[v], bonus ? 0.f : qr[v], v, key + (uint64_t)(v + 1) * kSmGamma);
     }
+    float bk = bt == INT_MAX ? INFINITY : be / bw;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
         const int ot = __shfl_xor_sync(0xffffffffu, bt, o);
         if (ok < bk || (ok == bk && ot < bt)) { bk = ok; bt = ot; }
-        const float op = __shfl_xor_sync(0xffffffffu, pm, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, pi, o);
-        if (better(op, oi, pm, pi)) { pm = op; pi = oi; }
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
     }
     __shared__ ChainPart sp[kChainThreads / 32];
+    __shared__ ChainPart s_r;
+    __shared__ int s_pidx;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) sp[warp] = ChainPart{bk, bt, pm, pi};
+    if (lane == 0) sp[warp] = ChainPart{bk, bt, pm, INT_MAX};
+    if (threadIdx.x == 0) s_pidx = INT_MAX;
     __syncthreads();
     if (threadIdx.x == 0) {
         ChainPart r = sp[0];
         for (int w = 1; w < kChainThreads / 32; ++w) {
             const ChainPart o = sp[w];
             if (o.key < r.key || (o.key == r.key && o.tok < r.tok)) { r.key = o.key; r.tok = o.tok; }
-            if (better(o.pmax, o.pidx, r.pmax, r.pidx)) { r.pmax = o.pmax; r.pidx = o.pidx; }
+            r.pmax = fmaxf(r.pmax, o.pmax);
         }
-        parts[(size_t)b * nchunk + c] = r;
+        s_r = r;
     }
+    __syncthreads();
+    ChainPart r = s_r;
+    if (r.tok == INT_MAX) {
+        // no positive weight in this chunk: the lowest token holding its largest
+        // p, for the fallback (rare; the chunk is read again)
+        for (int v = v0 + threadIdx.x; v < v1; v += kChainThreads)
+            if (pr[v] == r.pmax) { atomicMin(&s_pidx, v); break; }
+        __syncthreads();
+        r.pidx = s_pidx;
+    }
+    if (threadIdx.x == 0) parts[(size_t)b * nchunk + c] = r;
 }
 
 __global__ void __launch_bounds__(32) chain_finish_kernel(const ChainPart* __restrict__ parts,
