@@ -22,8 +22,17 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "topk.cuh"
 
 namespace medusa {
+
+// tensor-core heads for batches of 4 to 8 (heads_umma.cu)
+bool heads_umma_applies(int B, int K, int H, int V, int topk, bool bf16);
+size_t heads_umma_workspace(int B, int K, int H, int V, int topk);
+int launch_heads_umma(const void* h, const void* w1, const void* b1, const void* w2, int B, int K, int H,
+                      int V, int topk, int32_t* topk_idx, float* topk_val, float* logits, char* ws,
+                      cudaStream_t st);
+
 namespace {
 
 constexpr int kRows2 = 4;    // W2 rows a warp reduces together
@@ -207,33 +216,6 @@ __global__ void __launch_bounds__(THREADS) heads_w1_silu_kernel(
     }
 }
 
-// Selects, in `passes` rounds, the best remaining (value, index) pair among
-// n entries given by get(j) -> (value, index); one warp.  Writes through put().
-template <typename Get, typename Put>
-__device__ __forceinline__ void warp_select_topk(int n, int passes, Get get, Put put, int lane) {
-    float lastv = INFINITY;
-    int lasti = -1;
-    for (int t = 0; t < passes; ++t) {
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-        for (int j = lane; j < n; j += 32) {
-            float x;
-            int xi;
-            get(j, x, xi);
-            if (better(lastv, lasti, x, xi) && better(x, xi, bv, bi)) { bv = x; bi = xi; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-        }
-        if (lane == 0) put(t, bv, bi);
-        lastv = bv;
-        lasti = bi;
-    }
-}
-
 // K2: logits of one vocab slice of head k, then the slice's top-k per sequence.
 // The last CTA of head k to finish (elected with an atomic counter that K1
 // zeroed) merges the head's S slice lists into the final sorted top-k.
@@ -375,6 +357,10 @@ HeadsPlan plan_heads(int B, int K, int H, int V, int topk) {
     p.off_done = off;
     off = align_up(off + (size_t)K * sizeof(unsigned), 256);
     p.ws_bytes = off;
+    if (heads_umma_applies(B, K, H, V, topk, true)) {
+        const size_t u = heads_umma_workspace(B, K, H, V, topk);
+        if (u > p.ws_bytes) p.ws_bytes = u;
+    }
     return p;
 }
 
@@ -479,6 +465,10 @@ extern "C" int medusa_heads_topk(const void* h, const void* w1, const void* b1, 
         return fail(MEDUSA_ERR_UNSUPPORTED, "heads_topk: %zu bytes of shared memory needed", p.smem2);
     cudaStream_t st = as_stream(stream);
     char* w = static_cast<char*>(ws);
+    if (heads_umma_applies(B, K, H, V, topk, dtype == MEDUSA_BF16)) {
+        if (!aligned16(h)) return fail(MEDUSA_ERR_INVALID_ARG, "heads_topk: h must be 16-byte aligned");
+        return launch_heads_umma(h, w1, b1, w2, B, K, H, V, topk, topk_idx, topk_val, logits, w, st);
+    }
     if (dtype == MEDUSA_BF16)
         return dispatch_batch<uint16_t>(B, h, w1, b1, w2, K, H, V, topk, topk_idx, topk_val, logits,
                                         w, p, st);

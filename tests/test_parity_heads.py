@@ -24,6 +24,12 @@ def _run(M, x, topk):
     (3, 512, 3001, 5, 8, "bf16", 2e-2),
     (8, 1024, 2000, 2, 16, "bf16", 2e-2),
     (5, 264, 777, 4, 5, "f32", 1e-5),
+    # batches 4-8 in bf16 with H % 128 == 0 run on the tensor cores: ragged
+    # vocab tiles, 16 or 32 activation rows (3B), heads split across CTAs
+    (4, 256, 1000, 3, 8, "bf16", 2e-2),
+    (5, 384, 1337, 4, 8, "bf16", 2e-2),
+    (6, 640, 4099, 5, 8, "bf16", 2e-2),
+    (7, 128, 300, 6, 4, "bf16", 2e-2),
 ])
 def test_heads_small(medusa, B, H, V, K, topk, dtype, tol):
     x = W.heads_inputs(seed=B * 7 + K, B=B, H=H, V=V, K=K, dtype=dtype, b1_std=0.5)
