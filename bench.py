@@ -14,7 +14,8 @@ grows it) so every step sees the same workload.
 
 Beside the step, the JSON line carries "attention_workloads" (tree attention
 alone at the batch-8 ragged and batch-4 KV-8192 shapes), "chain_acceptance"
-(speculative-sampling acceptance at batch 64, vocab 128256) and
+(speculative-sampling acceptance at batch 64, vocab 128256), "heads_batches"
+(the heads alone at batch 4 and 8, on the tensor cores) and
 "verify_projection": the fused
 verification projection (lm_head x tree hidden states on the tensor cores,
 reduced to acceptance without writing logits) timed at the step's shapes and at
@@ -51,7 +52,7 @@ WORKLOAD = ("vicuna7b-shaped medusa step, batch 1: hidden 4096, vocab 32000, 5 h
 # DRAM bytes per launch of the heads call, from the ncu capture summarised in
 # profiles/ (dram__bytes_read.sum + dram__bytes_write.sum summed over its three
 # kernels), with the sha1 of heads.cu it was taken on; null once that file changes.
-HEADS_TRAFFIC = {"sha1": "3f0b467a704b63b419fb7cc805600417ab27a526", "bytes": 1479551933}
+HEADS_TRAFFIC = {"sha1": "63c732a5118f62fb6b71bf76462b5720cf109c08", "bytes": 1479545387}
 
 
 def _sha1(path):
@@ -394,6 +395,44 @@ def measure_attention_workloads(dev, iters=20, warmup=3):
     return out
 
 
+def measure_heads_batches(dev, iters=10, warmup=2):
+    """medusa_heads_topk alone at batch 4 (hidden 4096) and batch 8 (hidden 5120),
+    5 heads, vocab 32000, top-8, bf16 (random-init weights of those shapes; the
+    weights exceed L2), timed over `iters` back-to-back calls."""
+    import torch
+    import medusa_speculative_decoding_gb300 as M
+    hbm, _ = _peaks()
+    out = {}
+    for B, H in ((4, 4096), (8, 5120)):
+        K, V, topk = 5, 32000, 8
+        g = torch.Generator(device=dev)
+        g.manual_seed(11)
+        h = torch.randn(B, H, device=dev, generator=g).bfloat16()
+        w1 = (torch.randn(K, H, H, device=dev, generator=g) * 0.02).bfloat16()
+        b1 = torch.zeros(K, H, device=dev).bfloat16()
+        w2 = (torch.randn(K, V, H, device=dev, generator=g) * 0.02).bfloat16()
+        ws = torch.empty(M.heads_topk_workspace(B, K, H, V, topk), dtype=torch.uint8, device=dev)
+        res = (torch.empty(B, K, topk, dtype=torch.int32, device=dev),
+               torch.empty(B, K, topk, device=dev), None)
+        call = lambda: M.heads_topk(h, w1, b1, w2, topk, out=res, ws=ws)
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            call()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / iters
+        by = K * (H * H + H + V * H) * 2 + B * H * 2 + B * K * topk * 8
+        out[f"b{B}_h{H}"] = {"us": us, "gbs": by / (us * 1e-6) / 1e9, "frac_hbm": by / (us * 1e-6) / 1e9 / hbm,
+                             "algorithmic_bytes": by,
+                             "path": "tcgen05" if B >= 4 else "cuda cores"}
+        del h, w1, b1, w2, ws
+    return out
+
+
 def measure_chain(dev, gammas=(1, 4, 8, 32), sigma=0.5, reps=10):
     """medusa_verify_accept_chain at batch 64, vocab 128256 (the speculative-
     sampling sweep's shape): q = softmax(ql), p = softmax(ql + N(0, sigma)),
@@ -617,6 +656,7 @@ def main():
     proj = measure_projection(dev) if world == 1 or rank == 0 else None
     att_w = measure_attention_workloads(dev) if world == 1 or rank == 0 else None
     chain = measure_chain(dev) if world == 1 or rank == 0 else None
+    heads_b = measure_heads_batches(dev) if world == 1 or rank == 0 else None
 
     peak, peak_kind = _peaks()
     hb, ab, vb = algorithmic_bytes(c, N, int(inp["kv_len"][0]) + N)
@@ -642,6 +682,7 @@ def main():
             "verify_projection": proj,
             "attention_workloads": att_w,
             "chain_acceptance": chain,
+            "heads_batches": heads_b,
             "clocks": clocks,
             "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
