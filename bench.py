@@ -12,7 +12,8 @@ with every input resident in HBM.  The step reads ~1.52 GB, more than L2, so
 consecutive steps start cold.  kv_len is restored before each step (compaction
 grows it) so every step sees the same workload.
 
-Beside the step, the JSON line carries "attention_workloads" (tree attention
+Beside the step, the JSON line carries "step_graph_32_layers" (the step as one
+CUDA graph with tree attention over 32 layers' caches), "attention_workloads" (tree attention
 alone at the batch-8 ragged and batch-4 KV-8192 shapes), "chain_acceptance"
 (speculative-sampling acceptance at batch 64, vocab 128256), "heads_batches"
 (the heads alone at batch 4 and 8, on the tensor cores) and
@@ -395,6 +396,66 @@ def measure_attention_workloads(dev, iters=20, warmup=3):
     return out
 
 
+def measure_step_graph(step, layers=32, iters=200, warmup=5):
+    """The decode step as one CUDA graph with tree attention over `layers`
+    layers (each with its own KV cache; a stand-in for the backbone's attention
+    layers, whose other work is not part of this path): heads -> build_tree ->
+    layers x tree_attention -> verify -> one compaction of every layer's cache.
+    The caches are one tensor [B, layers * Hkv, Lmax, D], so layer l is heads
+    l*Hkv .. (l+1)*Hkv and one compaction call moves all layers' rows.  Reports
+    graph replays per second and accepted tokens per second (accept_len + 1
+    tokens per round)."""
+    import torch
+    M, c = step.M, CFG
+    dev = step.kc.device
+    B, Hkv, D = c["B"], c["Hkv"], c["D"]
+    Lmax = step.kc.shape[2]
+    if B != 1:
+        return None
+    kc = torch.empty((B, layers * Hkv, Lmax, D), dtype=step.kc.dtype, device=dev)
+    vc = torch.empty_like(kc)
+    for l in range(layers):  # every layer starts from the step's own cache
+        kc[:, l * Hkv:(l + 1) * Hkv].copy_(step.kc)
+        vc[:, l * Hkv:(l + 1) * Hkv].copy_(step.vc)
+    kls = [kc[:, l * Hkv:(l + 1) * Hkv] for l in range(layers)]
+    vls = [vc[:, l * Hkv:(l + 1) * Hkv] for l in range(layers)]
+
+    def one():
+        step.kv_len.copy_(step.kv_len0)
+        step.heads()
+        M.build_tree(step.idx, step.root, step.depth, step.rank, out=step.cand)
+        for l in range(layers):
+            M.tree_attention(step.q, kls[l], vls[l], step.kv_len, step.mask, out=step.att_out, ws=step.ws_att)
+        M.verify_accept_tree(step.vlogits, step.cand, step.parent, step.depth, step.Dmax, out=step.acc,
+                             ws=step.ws_ver)
+        M.kv_compact(kc, vc, step.kv_len, step.acc["path_nodes"], step.acc["accept_len"], step.acc["best_node"],
+                     step.N, step.Dmax, hidden_tree=step.ht, h_next=step.h_next, src_idx=step.src)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            one()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        one()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / iters
+    tokens = float(step.acc["accept_len"].float().mean().item()) + 1.0
+    del kc, vc
+    return {"layers": layers, "us_per_step": us, "steps_per_s": 1e6 / us, "tokens_per_step": tokens,
+            "tokens_per_s": tokens * 1e6 / us, "launches_per_step": 2 + 1 + layers + 2 + 1}
+
+
 def measure_heads_batches(dev, iters=10, warmup=2):
     """medusa_heads_topk alone at batch 4 (hidden 4096) and batch 8 (hidden 5120),
     5 heads, vocab 32000, top-8, bf16 (random-init weights of those shapes; the
@@ -653,6 +714,7 @@ def main():
     e2e_s, h2d, d2h = run_e2e(step, max(20, K // 4), args.warmup)
     e2e_val = world * max(20, K // 4) / e2e_s
 
+    graph = measure_step_graph(step) if world == 1 or rank == 0 else None
     proj = measure_projection(dev) if world == 1 or rank == 0 else None
     att_w = measure_attention_workloads(dev) if world == 1 or rank == 0 else None
     chain = measure_chain(dev) if world == 1 or rank == 0 else None
@@ -679,6 +741,7 @@ def main():
             "attention": {"achieved": att_gbs, "unit": "GB/s", "frac": att_gbs / peak,
                           "algorithmic_bytes": ab, "ms": att_ms},
             "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
+            "step_graph_32_layers": graph,
             "verify_projection": proj,
             "attention_workloads": att_w,
             "chain_acceptance": chain,
