@@ -564,6 +564,37 @@ int oracle_verify_chain(const float* p /* [B,gamma+1,V] */, const float* q /* [B
 /* into a temporary before any is written, so overlapping moves are safe.     */
 /* elem = bytes per element (4 fp32, 2 bf16).                                 */
 /* ------------------------------------------------------------------------- */
+/* O4s: typical acceptance with a sampled next token [MH, "Tree attention and */
+/* acceptance": in sampling, Medusa uses typical acceptance].  The accepted   */
+/* branch is the one oracle_verify_tree finds in typical mode; the token after */
+/* it is drawn from the base model's distribution at the best node,           */
+/* P = softmax(row / T), by the exponential race above with weights           */
+/* w_v = exp(row_v / T - max / T) and row key stream 4, pos 0.                */
+/* ------------------------------------------------------------------------- */
+int oracle_verify_tree_sample(const float* logits, const int32_t* cand, const int32_t* parent,
+                              const int32_t* depth, int B, int N, int V, int Dmax, double T, double eps,
+                              double delta, uint64_t seed, uint64_t round, int32_t* accept_len,
+                              int32_t* best_node, int32_t* path_nodes, int32_t* next_tok,
+                              double* race_gap /* [B] or NULL */) {
+    if (!(T > 0)) return OR_EINVAL;
+    int rc = oracle_verify_tree(logits, cand, parent, depth, B, N, V, Dmax, 1, T, eps, delta, accept_len,
+                                best_node, path_nodes, next_tok, NULL, NULL, NULL, NULL);
+    if (rc != OR_OK) return rc;
+    double* w = (double*)malloc((size_t)V * sizeof(double));
+    if (!w) return OR_ENOMEM;
+    for (int b = 0; b < B; ++b) {
+        const float* row = logits + ((size_t)b * N + best_node[b]) * V;
+        double mx = -INFINITY;
+        for (int v = 0; v < V; ++v) if ((double)row[v] / T > mx) mx = (double)row[v] / T;
+        for (int v = 0; v < V; ++v) w[v] = exp((double)row[v] / T - mx);
+        next_tok[b] = race(w, row, V, oracle_row_key(seed, 4, (uint64_t)b, round, 0),
+                           race_gap ? race_gap + b : NULL);
+    }
+    free(w);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
 int oracle_kv_compact(void* kc, void* vc, int elem, int32_t* kv_len, const int32_t* path_nodes,
                       const int32_t* accept_len, const int32_t* best_node, const void* hidden_tree,
                       void* h_next, int B, int Hkv, int D, int Lmax, int N, int H, int Dmax,

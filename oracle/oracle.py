@@ -34,6 +34,8 @@ def lib():
         L.oracle_verify_tree.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, dbl, dbl, dbl,
                                          P, P, P, P, P, P, P, P]
         L.oracle_verify_chain.argtypes = [P, P, P, i32, i32, i32, u64, u64, P, P, P]
+        L.oracle_verify_tree_sample.argtypes = [P, P, P, P, i32, i32, i32, i32, dbl, dbl, dbl, u64, u64,
+                                                P, P, P, P, P]
         L.oracle_kv_compact.argtypes = [P, P, i32, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                         i32, i32, P]
         L.oracle_splitmix64.argtypes = [u64, u64]
@@ -215,6 +217,24 @@ def verify_chain(p, q, draft, seed, round_):
                                      C.c_uint64(seed), C.c_uint64(round_), _p(n_acc), _p(out),
                                      _p(gap)), "verify_chain")
     return dict(n_acc=n_acc, out_tok=out, race_gap=gap)
+
+
+def verify_tree_sample(logits, cand, parent, depth, max_depth, seed, round_, T=1.0, eps=0.09,
+                       delta=0.3):
+    """Typical acceptance; the next token drawn from softmax(row_best / T)."""
+    logits = _c(logits, np.float32)
+    cand, parent, depth = _c(cand, np.int32), _c(parent, np.int32), _c(depth, np.int32)
+    B, N, V = logits.shape
+    r = dict(accept_len=np.zeros(B, np.int32), best_node=np.zeros(B, np.int32),
+             path_nodes=np.zeros((B, max_depth + 1), np.int32), next_tok=np.zeros(B, np.int32),
+             race_gap=np.zeros(B, np.float64))
+    _check(lib().oracle_verify_tree_sample(_p(logits), _p(cand), _p(parent), _p(depth), B, N, V,
+                                           max_depth, T, eps, delta, C.c_uint64(seed),
+                                           C.c_uint64(round_), _p(r["accept_len"]),
+                                           _p(r["best_node"]), _p(r["path_nodes"]),
+                                           _p(r["next_tok"]), _p(r["race_gap"])),
+           "verify_tree_sample")
+    return r
 
 
 def splitmix64(state, n):

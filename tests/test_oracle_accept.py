@@ -133,3 +133,45 @@ def test_typical_with_huge_threshold_scale_equals_greedy_on_planted_rows():
     ty = O.verify_tree(logits, cand, t["parent"], t["depth"], t["max_depth"], "typical", 1.0, 0.5, 1.0)
     for k in ("accept_len", "best_node", "path_nodes", "next_tok"):
         assert np.array_equal(g[k], ty[k])
+
+
+# ---------------------------------------------------------------------------
+# typical acceptance with a sampled next token (Medusa Heads glossary page,
+# "Tree attention and acceptance": in sampling, Medusa uses typical acceptance)
+# ---------------------------------------------------------------------------
+def test_sampled_next_token_follows_the_softmax_of_the_best_row():
+    # root-only tree: the best node is the root, so the token after it is a
+    # draw from softmax(row0 / T); many rounds of the counter-based generator
+    # must reproduce that distribution (chi-square), for two temperatures
+    t = O.tree_layout(np.zeros((0, 1), np.int32), 1)
+    V = 7
+    x = np.array([[[1.5, -0.3, 0.2, 2.0, -1.0, 0.7, 0.0]]], np.float32)
+    cand = np.zeros((1, t["N"]), np.int32)
+    R = 12000
+    for T in (1.0, 0.6):
+        draws = np.array([O.verify_tree_sample(x, cand, t["parent"], t["depth"], t["max_depth"], 9, r, T)
+                          ["next_tok"][0] for r in range(R)])
+        expect = scipy.special.softmax(x[0, 0].astype(np.float64) / T) * R
+        counts = np.bincount(draws, minlength=V)
+        assert scipy.stats.chisquare(counts, expect).pvalue > 1e-3
+
+
+def test_sampled_next_token_keeps_the_typical_branch_and_cools_to_argmax():
+    t = _tree("sparse64")
+    B, V = 3, 500
+    cand = _cands(t, B, V, seed=90, K=5)
+    logits = W.normal_logits(90, B, t["N"], V, 3.0)
+    typ = O.verify_tree(logits, cand, t["parent"], t["depth"], t["max_depth"], "typical", 1.0)
+    smp = O.verify_tree_sample(logits, cand, t["parent"], t["depth"], t["max_depth"], 5, 0, 1.0)
+    for key in ("accept_len", "best_node", "path_nodes"):
+        assert np.array_equal(smp[key], typ[key])
+    # a vanishing temperature leaves one positive weight: the row's argmax
+    cold = O.verify_tree_sample(logits, cand, t["parent"], t["depth"], t["max_depth"], 5, 0, 1e-4)
+    best_rows = logits[np.arange(B), cold["best_node"]]
+    assert np.array_equal(cold["next_tok"], best_rows.argmax(-1))
+    # the same (seed, round) draws the same token; other rounds draw others
+    again = O.verify_tree_sample(logits, cand, t["parent"], t["depth"], t["max_depth"], 5, 0, 1.0)
+    assert np.array_equal(again["next_tok"], smp["next_tok"])
+    many = {int(O.verify_tree_sample(logits, cand, t["parent"], t["depth"], t["max_depth"], 5, r, 1.0)
+                ["next_tok"][0]) for r in range(40)}
+    assert len(many) > 1
