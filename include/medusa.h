@@ -198,6 +198,25 @@ int medusa_verify_accept_tree(const float* logits, const int32_t* cand, const in
                               size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* 4b'. Typical acceptance with a sampled next token  [MH, "Tree attention    */
+/*      and acceptance": in sampling, Medusa uses typical acceptance]         */
+/*                                                                           */
+/* accept_len, best_node and path_nodes as medusa_verify_accept_tree in      */
+/* MEDUSA_ACCEPT_TYPICAL mode.  next_tok is drawn from P = softmax(row / T)   */
+/* of the best node by the exponential race argmin_v -ln(U+(h_v)) / w_v,      */
+/* w_v = exp(row_v / T - max / T), lowest v on ties, with the SplitMix64      */
+/* keys of 4b: key = f(f(f(f(f(seed) ^ 4) ^ b) ^ round) ^ 0), h_v =           */
+/* next(key, v + 1).  Workspace from medusa_verify_sample_workspace.          */
+/* ------------------------------------------------------------------------- */
+size_t medusa_verify_sample_workspace(int B, int N, int V);
+int medusa_verify_accept_tree_sample(const float* logits, const int32_t* cand, const int32_t* parent,
+                                     const int32_t* depth, int B, int N, int V, int Dmax,
+                                     float temperature, float eps, float delta, uint64_t seed,
+                                     uint64_t round, int32_t* accept_len, int32_t* best_node,
+                                     int32_t* path_nodes, int32_t* next_tok, void* ws,
+                                     size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* 4c. Verification projection fused with tree acceptance  [MH, "Tree         */
 /*     attention and acceptance": the base model scores every branch of the   */
 /*     tree in one pass]                                                      */

@@ -10,7 +10,9 @@ the C ABI of include/medusa.h); this package is its thin Python binding:
   build_tree          candidate tokens of the tree nodes
   tree_attention      ancestor-masked attention of all candidates in one pass
   verify_accept_tree  greedy / typical acceptance, longest accepted branch
-  verify_project_tree the same from the tree's hidden states: lm_head projection
+  verify_accept_tree_sample  typical acceptance, next token drawn from the
+                      best node's softmax
+  verify_project_tree the same as verify_accept_tree from the tree's hidden states: lm_head projection
                       on the tensor cores, reduced without writing the logits
   verify_accept_chain speculative-sampling acceptance with k + 1 tokens
   kv_compact          keep the accepted branch's KV rows and hidden state
@@ -20,4 +22,5 @@ from .api import (build_tree, heads_topk, heads_topk_static, heads_topk_workspac
                   kv_compact,
                   sparse_tree_paths, tree_attention, tree_attention_workspace, tree_layout,
                   verify_accept_chain, verify_accept_tree, verify_accept_workspace,
-                  verify_chain_workspace, verify_project_tree, verify_project_workspace)
+                  verify_accept_tree_sample, verify_chain_workspace, verify_project_tree,
+                  verify_project_workspace, verify_sample_workspace)

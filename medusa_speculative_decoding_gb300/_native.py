@@ -22,6 +22,7 @@ EXPORTS = (
     "medusa_tree_attention_workspace", "medusa_tree_attention",
     "medusa_verify_accept_workspace", "medusa_verify_accept_tree",
     "medusa_verify_project_workspace", "medusa_verify_project_tree",
+    "medusa_verify_sample_workspace", "medusa_verify_accept_tree_sample",
     "medusa_verify_chain_workspace", "medusa_verify_accept_chain",
     "medusa_kv_compact",
 )
@@ -65,6 +66,10 @@ def lib() -> C.CDLL:
     L.medusa_verify_project_workspace.restype = sz
     L.medusa_verify_project_tree.argtypes = [P, P, i32, P, P, P, i32, i32, i32, i32, i32, i32, f32,
                                              f32, f32, P, P, P, P, P, sz, P]
+    L.medusa_verify_sample_workspace.argtypes = [i32] * 3
+    L.medusa_verify_sample_workspace.restype = sz
+    L.medusa_verify_accept_tree_sample.argtypes = [P, P, P, P, i32, i32, i32, i32, f32, f32, f32, u64, u64,
+                                                   P, P, P, P, P, sz, P]
     L.medusa_verify_chain_workspace.argtypes = [i32] * 3
     L.medusa_verify_chain_workspace.restype = sz
     L.medusa_verify_accept_chain.argtypes = [P, P, P, i32, i32, i32, u64, u64, P, P, P, sz, P]

@@ -197,6 +197,35 @@ def verify_accept_tree(logits, cand, parent, depth, max_depth, mode="greedy", te
     return out
 
 
+def verify_sample_workspace(B, N, V):
+    return int(lib().medusa_verify_sample_workspace(B, N, V))
+
+
+def verify_accept_tree_sample(logits, cand, parent, depth, max_depth, seed, round_, temperature=1.0,
+                              eps=0.09, delta=0.3, out=None, ws=None, stream=None):
+    """Typical acceptance; the next token drawn from the best node's softmax."""
+    _need(logits, "logits", torch.float32)
+    _need(cand, "cand", torch.int32)
+    _need(parent, "parent", torch.int32)
+    _need(depth, "depth", torch.int32)
+    B, N, V = logits.shape
+    dev = logits.device
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   best_node=torch.empty(B, dtype=torch.int32, device=dev),
+                   path_nodes=torch.empty((B, max_depth + 1), dtype=torch.int32, device=dev),
+                   next_tok=torch.empty(B, dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = _ws(verify_sample_workspace(B, N, V), dev)
+    check(lib().medusa_verify_accept_tree_sample(_ptr(logits), _ptr(cand), _ptr(parent), _ptr(depth), B, N,
+                                                 V, max_depth, float(temperature), float(eps), float(delta),
+                                                 C.c_uint64(seed), C.c_uint64(round_),
+                                                 _ptr(out["accept_len"]), _ptr(out["best_node"]),
+                                                 _ptr(out["path_nodes"]), _ptr(out["next_tok"]), _ptr(ws),
+                                                 ws.numel(), _stream(stream)))
+    return out
+
+
 def verify_project_workspace(B, N, H, V):
     return int(lib().medusa_verify_project_workspace(B, N, H, V))
 

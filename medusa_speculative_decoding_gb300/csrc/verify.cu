@@ -7,6 +7,8 @@
 //   row_stats_kernel   : one pass over each verifier-logits chunk (HBM-bound):
 //                        argmax, and for typical acceptance the running
 //                        (max, sum exp, sum exp * x) of x = logit / T
+//   tree_race_kernel, tree_race_finish_kernel : (sampled next token) the
+//                        exponential race over the best node's softmax
 //   accept_tree_kernel : per sequence: merge chunk stats, test each candidate
 //                        against its parent's row, AND along ancestors, pick the
 //                        deepest accepted node (lowest index on ties); also the
@@ -395,6 +397,89 @@ size_t verify_ws(int B, int N, int V) {
     return align_up((size_t)B * N * nchunk * sizeof(RowStat), 256);
 }
 
+// ---------------------------------------------------------------------------
+// Typical acceptance with a sampled next token: after the acceptance kernel
+// has picked the best node, the token after it is drawn from softmax(row / T)
+// of that node by the exponential race (weights exp(x - m), x = logit / T, m
+// the row maximum from the statistics; SplitMix64 row key stream 4, pos 0).
+// ---------------------------------------------------------------------------
+constexpr int kRaceChunk = 4096;
+constexpr int kRaceThreads = 256;
+
+struct RacePart {
+    float key;
+    int tok;
+};
+
+__global__ void __launch_bounds__(kRaceThreads) tree_race_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ best_node, const RowStat* __restrict__ stats,
+    int N, int V, int nchunk_stats, float inv_t, uint64_t seed, uint64_t round, int nchunk,
+    RacePart* __restrict__ parts) {
+    pdl_wait();
+    pdl_trigger();
+    const int c = blockIdx.x, b = blockIdx.y;
+    const int best = best_node[b];
+    float be = INFINITY, bw = 1.f;  // best key as the fraction be / bw
+    int bt = INT_MAX;
+    if (best >= 0 && best < N) {
+        const RowStat* st = stats + ((size_t)b * N + best) * nchunk_stats;
+        float m = -INFINITY;
+        for (int k = 0; k < nchunk_stats; ++k) m = fmaxf(m, st[k].m);
+        const float* row = logits + ((size_t)b * N + best) * V;
+        const uint64_t key = row_key(seed, 4, b, round, 0);
+        const int v0 = c * kRaceChunk, v1 = min(V, v0 + kRaceChunk);
+        for (int v = v0 + threadIdx.x; v < v1; v += kRaceThreads) {
+            const float w = expf(row[v] * inv_t - m);
+            if (w > 0.f) {
+                const float e = -logf(u24p(sm_mix(key + (uint64_t)(v + 1) * kSmGamma)));
+                const float lhs = e * bw, rhs = be * w;
+                if (lhs < rhs || (lhs == rhs && v < bt)) { be = e; bw = w; bt = v; }
+            }
+        }
+    }
+    float bk = bt == INT_MAX ? INFINITY : be / bw;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        const int ot = __shfl_xor_sync(0xffffffffu, bt, o);
+        if (ok < bk || (ok == bk && ot < bt)) { bk = ok; bt = ot; }
+    }
+    __shared__ RacePart sp[kRaceThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) sp[warp] = RacePart{bk, bt};
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        RacePart r = sp[0];
+        for (int w = 1; w < kRaceThreads / 32; ++w)
+            if (sp[w].key < r.key || (sp[w].key == r.key && sp[w].tok < r.tok)) r = sp[w];
+        parts[(size_t)b * nchunk + c] = r;
+    }
+}
+
+// One warp per sequence: the chunks' winners merged into next_tok (left as the
+// argmax the acceptance kernel wrote when no weight is positive).
+__global__ void __launch_bounds__(32) tree_race_finish_kernel(const RacePart* __restrict__ parts, int nchunk,
+                                                              const int32_t* __restrict__ best_node, int N,
+                                                              int32_t* __restrict__ next_tok) {
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x, lane = threadIdx.x;
+    float bk = INFINITY;
+    int bt = INT_MAX;
+    for (int c = lane; c < nchunk; c += 32) {
+        const RacePart r = parts[(size_t)b * nchunk + c];
+        if (r.key < bk || (r.key == bk && r.tok < bt)) { bk = r.key; bt = r.tok; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        const int ot = __shfl_xor_sync(0xffffffffu, bt, o);
+        if (ok < bk || (ok == bk && ot < bt)) { bk = ok; bt = ot; }
+    }
+    const int best = best_node[b];
+    if (lane == 0 && bt != INT_MAX && best >= 0 && best < N) next_tok[b] = bt;
+}
+
 constexpr int kFinishWarps = 8;
 
 // One warp per row: lanes merge the row's split records, then a shuffle tree
@@ -568,6 +653,51 @@ extern "C" int medusa_verify_accept_tree(const float* logits, const int32_t* can
     aa.path_nodes = path_nodes;
     aa.next_tok = next_tok;
     return launch_accept_tree(mode == MEDUSA_ACCEPT_TYPICAL, aa, st);
+}
+
+extern "C" size_t medusa_verify_sample_workspace(int B, int N, int V) {
+    if (B < 1 || N < 1 || V < 1) return 0;
+    const int nrace = (V + kRaceChunk - 1) / kRaceChunk;
+    return align_up(verify_ws(B, N, V) + (size_t)B * nrace * sizeof(RacePart), 256);
+}
+
+extern "C" int medusa_verify_accept_tree_sample(const float* logits, const int32_t* cand,
+                                                const int32_t* parent, const int32_t* depth, int B, int N,
+                                                int V, int Dmax, float temperature, float eps, float delta,
+                                                uint64_t seed, uint64_t round, int32_t* accept_len,
+                                                int32_t* best_node, int32_t* path_nodes,
+                                                int32_t* next_tok, void* ws, size_t ws_bytes,
+                                                void* stream) {
+    if (!logits || !cand || !parent || !depth || !accept_len || !best_node || !path_nodes || !next_tok)
+        return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_tree_sample: null pointer");
+    if (B < 1 || N < 1 || V < 1 || Dmax < 0)
+        return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_tree_sample: bad sizes");
+    if (N > kAcceptThreads || B > 65535 || (long long)B * N > 65535)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "verify_accept_tree_sample: N=%d above %d or B*N above 65535", N,
+                    kAcceptThreads);
+    if (!(temperature > 0.f))
+        return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_tree_sample: temperature must be > 0");
+    const size_t need = medusa_verify_sample_workspace(B, N, V);
+    if (!ws || ws_bytes < need)
+        return fail(MEDUSA_ERR_WORKSPACE, "verify_accept_tree_sample: workspace of %zu bytes needed, %zu given",
+                    need, ws ? ws_bytes : (size_t)0);
+    if (!aligned16(ws)) return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_tree_sample: ws must be 16-byte aligned");
+    int rc = medusa_verify_accept_tree(logits, cand, parent, depth, B, N, V, Dmax, MEDUSA_ACCEPT_TYPICAL,
+                                       temperature, eps, delta, accept_len, best_node, path_nodes, next_tok, ws,
+                                       ws_bytes, stream);
+    if (rc) return rc;
+    const int nstat = (V + kChunk - 1) / kChunk;
+    const int nrace = (V + kRaceChunk - 1) / kRaceChunk;
+    RacePart* parts = reinterpret_cast<RacePart*>(static_cast<char*>(ws) + verify_ws(B, N, V));
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e = launch(tree_race_kernel, dim3(nrace, B), dim3(kRaceThreads), 0, st, logits,
+                           (const int32_t*)best_node, (const RowStat*)ws, N, V, nstat, 1.f / temperature, seed,
+                           round, nrace, parts);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "tree_race: launch failed: %s", cudaGetErrorString(e));
+    e = launch(tree_race_finish_kernel, dim3(B), dim3(32), 0, st, (const RacePart*)parts, nrace,
+               (const int32_t*)best_node, N, next_tok);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "tree_race_finish: launch failed: %s", cudaGetErrorString(e));
+    return MEDUSA_OK;
 }
 
 extern "C" size_t medusa_verify_chain_workspace(int B, int gamma, int V) {

@@ -126,3 +126,36 @@ def test_typical_special_cases(medusa):
     assert (got["accept_len"] == 0).all() and (got["best_node"] == 0).all()
     # k + 1 tokens: accept_len + 1 >= 1 always; path root..best
     assert (got["path_nodes"][:, 0] == 0).all()
+
+
+@pytest.mark.parametrize("kind,B,V,T", [("c1", 2, 1000, 1.0), ("sparse64", 4, 32000, 1.0),
+                                        ("sparse64", 3, 4099, 0.7), ("dense", 2, 5003, 1.0)])
+def test_typical_sampled_next_token_matches_oracle(medusa, kind, B, V, T):
+    # accept outputs as typical acceptance; the next token is the oracle's own
+    # exponential-race draw from the best node's softmax, except where the
+    # oracle's two best race keys are within 1e-5 relative (counted)
+    t = _tree(kind)
+    K, k = (3, 3) if kind == "c1" else ((4, 4) if kind == "dense" else (5, 8))
+    cand = _cands(t, B, V, seed=95, K=K, k=k)
+    logits = W.normal_logits(95, B, t["N"], V, 3.0)
+    typ = O.verify_tree(logits, cand, t["parent"], t["depth"], t["max_depth"], "typical", T)
+    ties = 0
+    for rnd in range(3):
+        r = medusa.verify_accept_tree_sample(to_dev(logits), to_dev(cand), to_dev(t["parent"]),
+                                             to_dev(t["depth"]), t["max_depth"], 31, rnd, T)
+        torch.cuda.synchronize()
+        got = {kk: to_np(v) for kk, v in r.items()}
+        ref = O.verify_tree_sample(logits, cand, t["parent"], t["depth"], t["max_depth"], 31, rnd, T)
+        amb = 0
+        for b in range(B):
+            tau = typ["tau"][b, t["parent"][1:]]
+            if (np.abs(typ["pcand"][b, 1:] - tau) <= 1e-4 * tau).any():
+                amb += 1
+                continue
+            for key in ("accept_len", "best_node", "path_nodes"):
+                assert np.array_equal(got[key][b], ref[key][b]), (key, b)
+            if got["next_tok"][b] != ref["next_tok"][b]:
+                assert ref["race_gap"][b] < 1e-5, (b, got["next_tok"][b], ref["next_tok"][b])
+                ties += 1
+        assert amb <= 1
+    assert ties <= 1
