@@ -78,6 +78,10 @@ int medusa_abi_version(void);
 /*   logits   [B,K,V]    float    out, may be NULL (skips the write)           */
 /* Limits: 1 <= B <= 8, 1 <= K <= 64, 8 <= H <= 16384 with H % 8 == 0,         */
 /* B * H <= 49152, topk <= 16, topk <= V.  Work is split over the vocab.      */
+/* bf16 batches of 4 to 8 with H % 128 == 0 run on the tensor cores (z is     */
+/* carried as three bf16 planes that hold 24 significant bits); h must then   */
+/* be 16-byte aligned.  If a device-side wait gives up there (about one       */
+/* second), the affected topk_idx entries are -1.                             */
 /* ------------------------------------------------------------------------- */
 size_t medusa_heads_topk_workspace(int B, int K, int H, int V, int topk);
 int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void* w2,
@@ -162,6 +166,9 @@ int medusa_build_tree(const int32_t* topk_idx, const int32_t* root_tok, const in
 /*   out     [B,N,Hq,D] float32                                               */
 /* Query head hq reads KV head hq / (Hq / Hkv).  Limits: D in {64, 128},      */
 /* 1 <= N <= 512, Hq % Hkv == 0, N * (Hq/Hkv) <= 4096.                       */
+/* The bf16 path merges its KV-split partials on chip and needs no workspace: */
+/* medusa_tree_attention_workspace returns 0 and ws may be NULL.  If a        */
+/* device-side wait gives up (about one second), the affected outputs are NaN. */
 /* ------------------------------------------------------------------------- */
 size_t medusa_tree_attention_workspace(int B, int N, int Hq, int Hkv, int D, int Lmax);
 int medusa_tree_attention(const void* q, const void* k_cache, const void* v_cache,

@@ -3,8 +3,10 @@
 // scores position t + k + 1 through one residual SiLU layer and a vocab
 // projection).
 //
-// At decode batch sizes (B <= 8) both products are matrix-vector products over
-// weights that are read once per step, so the heads are bound by HBM bandwidth:
+// At decode batch sizes (B <= 8) both products read weights that are used once
+// per step, so the heads are bound by HBM bandwidth.  bf16 batches of 4 to 8
+// run on the tensor cores (heads_umma.cu); everything else runs here, on CUDA
+// cores, as matrix-vector products:
 //   K1 heads_w1_silu : z[b,k,:] = h[b] + SiLU(W1_k h[b] + b1_k)   (float32 z);
 //                      the K*H rows of W1 are split evenly over the warps of
 //                      one wave of CTAs
