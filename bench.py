@@ -706,6 +706,11 @@ def main():
     ms_total = max_over_ranks(start.elapsed_time(end), world, dev)
     call_ms = {name: statistics.mean(evs[i][c].elapsed_time(evs[i][c + 1]) for i in range(K))
                for c, name in enumerate(Step.CALLS)}
+    # per-step distribution from the event pass (events between the calls
+    # lengthen each step a little, so these run slightly above ms_per_step)
+    per_step = sorted(evs[i][0].elapsed_time(evs[i][5]) for i in range(K))
+    pct = lambda f: per_step[min(K - 1, int(f * K))]
+    step_dist = {"p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9), "with_call_events": True}
     heads_ms = call_ms["heads_topk"]
     att_ms = call_ms["tree_attention"]
     ms_step = ms_total / K
@@ -741,6 +746,7 @@ def main():
             "attention": {"achieved": att_gbs, "unit": "GB/s", "frac": att_gbs / peak,
                           "algorithmic_bytes": ab, "ms": att_ms},
             "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
+            "step_ms_distribution": step_dist,
             "step_graph_32_layers": graph,
             "verify_projection": proj,
             "attention_workloads": att_w,
