@@ -40,11 +40,14 @@ constexpr int kUThreads = 192;
 constexpr int kUA = kUM * kUK * 2;       // 16 KB of weight rows per stage
 constexpr int kUBmax = 32 * kUK * 2;     // 4 KB of activation rows per stage (N <= 32)
 constexpr int kUStage = kUA + kUBmax;
-constexpr int kUMaxItems = 8;            // W2 items one CTA may own
+constexpr int kUMaxItems = 16;           // W2 items one CTA may own
 constexpr int kUMaxB = 8;
 constexpr int kUTopk = 16;
 constexpr long long kUWait = 1ll << 31;  // ~1 s at 2 GHz
-constexpr int kW1Stages = 5, kW2Stages = 4;  // both kernels fit two CTAs per SM
+// W1: two CTAs per SM (its 160-200 tiles then need no second round); W2: one
+// CTA per SM with a deeper ring, so each SM's share of the 128-row items is
+// within one item of the mean
+constexpr int kW1Stages = 5, kW2Stages = 8;
 
 // ring | barriers | tmem slot, flags | (W2 only) tile logits and run staging
 template <int STAGES, bool STAGING>
@@ -265,7 +268,7 @@ __device__ __forceinline__ void head_ctas(int k, int T, int items, int grid, int
 }
 
 template <int NB>
-__global__ void __launch_bounds__(kUThreads, 2) heads_w2_umma_kernel(
+__global__ void __launch_bounds__(kUThreads, 1) heads_w2_umma_kernel(
     const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmz, W2Args a) {
     using namespace umma;
     extern __shared__ uint8_t smem_raw[];
@@ -397,8 +400,8 @@ int bf16_rows_map(CUtensorMap* m, const void* p, int H, long long rows, int box_
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// two CTAs per SM: the W2 items are dealt over this many CTAs
-int umma_grid() { return 2 * sm_count(); }
+// W2 items are dealt over one CTA per SM
+int umma_grid() { return sm_count(); }
 
 bool heads_umma_applies(int B, int K, int H, int V, int topk, bool bf16) {
     const int grid = umma_grid();
@@ -443,7 +446,7 @@ int launch_heads_umma(const void* h, const void* w1, const void* b1, const void*
             : B == 7 ? heads_w2_umma_kernel<7> : heads_w2_umma_kernel<8>;
     cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, W2Smem::kBytes);
     const int tiles1 = K * H / kUM;
-    cudaError_t e = launch(heads_w1_umma_kernel, dim3(min(grid, tiles1)), dim3(kUThreads), (size_t)W1Smem::kBytes, st,
+    cudaError_t e = launch(heads_w1_umma_kernel, dim3(min(2 * grid, tiles1)), dim3(kUThreads), (size_t)W1Smem::kBytes, st,
                            tw1, th, static_cast<const uint16_t*>(h), static_cast<const uint16_t*>(b1), B, K, H,
                            zp, done, status);
     if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "heads_w1_umma: launch failed: %s", cudaGetErrorString(e));
