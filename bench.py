@@ -16,7 +16,8 @@ Beside the step, the JSON line carries "step_graph_32_layers" (the step as one
 CUDA graph with tree attention over 32 layers' caches), "attention_workloads" (tree attention
 alone at the batch-8 ragged and batch-4 KV-8192 shapes), "chain_acceptance"
 (speculative-sampling acceptance at batch 64, vocab 128256), "heads_batches"
-(the heads alone at batch 4 and 8, on the tensor cores) and
+(a batch sweep of the heads alone: batch 1-64 at hidden 4096, batch 8 at
+hidden 5120) and
 "verify_projection": the fused
 verification projection (lm_head x tree hidden states on the tensor cores,
 reduced to acceptance without writing logits) timed at the step's shapes and at
@@ -457,40 +458,46 @@ def measure_step_graph(step, layers=32, iters=200, warmup=5):
 
 
 def measure_heads_batches(dev, iters=10, warmup=2):
-    """medusa_heads_topk alone at batch 4 (hidden 4096) and batch 8 (hidden 5120),
-    5 heads, vocab 32000, top-8, bf16 (random-init weights of those shapes; the
-    weights exceed L2), timed over `iters` back-to-back calls."""
+    """Batch sweep of medusa_heads_topk: hidden 4096 at batch 1, 2, 4, 8, 16, 32
+    and 64, and hidden 5120 at batch 8; 5 heads, vocab 32000, top-8, bf16
+    (random-init weights of those shapes, allocated once per hidden size; they
+    exceed L2), each point timed over `iters` back-to-back calls.  Batches 1-3
+    run on CUDA cores, 4-64 on the tensor cores."""
     import torch
     import medusa_speculative_decoding_gb300 as M
     hbm, _ = _peaks()
     out = {}
-    for B, H in ((4, 4096), (8, 5120)):
-        K, V, topk = 5, 32000, 8
+    K, V, topk = 5, 32000, 8
+    for H, batches in ((4096, (1, 2, 4, 8, 16, 32, 64)), (5120, (8,))):
         g = torch.Generator(device=dev)
         g.manual_seed(11)
-        h = torch.randn(B, H, device=dev, generator=g).bfloat16()
         w1 = (torch.randn(K, H, H, device=dev, generator=g) * 0.02).bfloat16()
         b1 = torch.zeros(K, H, device=dev).bfloat16()
         w2 = (torch.randn(K, V, H, device=dev, generator=g) * 0.02).bfloat16()
-        ws = torch.empty(M.heads_topk_workspace(B, K, H, V, topk), dtype=torch.uint8, device=dev)
-        res = (torch.empty(B, K, topk, dtype=torch.int32, device=dev),
-               torch.empty(B, K, topk, device=dev), None)
-        call = lambda: M.heads_topk(h, w1, b1, w2, topk, out=res, ws=ws)
-        for _ in range(warmup):
-            call()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(iters):
-            call()
-        b.record()
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / iters
-        by = K * (H * H + H + V * H) * 2 + B * H * 2 + B * K * topk * 8
-        out[f"b{B}_h{H}"] = {"us": us, "gbs": by / (us * 1e-6) / 1e9, "frac_hbm": by / (us * 1e-6) / 1e9 / hbm,
-                             "algorithmic_bytes": by,
-                             "path": "tcgen05" if B >= 4 else "cuda cores"}
-        del h, w1, b1, w2, ws
+        for B in batches:
+            h = torch.randn(B, H, device=dev, generator=g).bfloat16()
+            ws = torch.empty(M.heads_topk_workspace(B, K, H, V, topk), dtype=torch.uint8, device=dev)
+            res = (torch.empty(B, K, topk, dtype=torch.int32, device=dev),
+                   torch.empty(B, K, topk, device=dev), None)
+            call = lambda: M.heads_topk(h, w1, b1, w2, topk, out=res, ws=ws)
+            for _ in range(warmup):
+                call()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(iters):
+                call()
+            b.record()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / iters
+            by = K * (H * H + H + V * H) * 2 + B * H * 2 + B * K * topk * 8
+            fl = 2.0 * B * K * (H * H + V * H)
+            out[f"b{B}_h{H}"] = {"us": us, "gbs": by / (us * 1e-6) / 1e9,
+                                 "frac_hbm": by / (us * 1e-6) / 1e9 / hbm, "algorithmic_bytes": by,
+                                 "tflops": fl / (us * 1e-6) / 1e12, "sequences_per_s": B * 1e6 / us,
+                                 "path": "tcgen05" if B >= 4 else "cuda cores"}
+            del h, ws
+        del w1, b1, w2
     return out
 
 

@@ -332,6 +332,10 @@ struct HeadsPlan {
 
 HeadsPlan plan_heads(int B, int K, int H, int V, int topk) {
     HeadsPlan p{};
+    if (B > 8) {  // tensor cores only
+        p.ws_bytes = heads_umma_workspace(B, K, H, V, topk);
+        return p;
+    }
     const size_t xbytes = (size_t)B * H * sizeof(float);
     const bool big = xbytes > 64 * 1024;
     p.threads = big ? 512 : 256;
@@ -427,11 +431,14 @@ int check_heads_shapes(int B, int K, int H, int V, int topk) {
     if (B < 1 || K < 1 || H < 1 || V < 1 || topk < 1)
         return fail(MEDUSA_ERR_INVALID_ARG, "heads_topk: sizes must be positive (B=%d K=%d H=%d V=%d topk=%d)",
                     B, K, H, V, topk);
-    if (B > 8 || K > 64 || H < 8 || H > 16384 || H % 8 || (long long)B * H > 49152 || topk > 16 ||
-        topk > V)
+    // batches 9-64 exist only on the tensor cores (bf16, H % 128 == 0)
+    const bool wide_ok = B > 8 && B <= 64 && heads_umma_applies(B, K, H, V, topk, true);
+    if ((B > 8 && !wide_ok) || K > 64 || H < 8 || H > 16384 || H % 8 || (B <= 8 && (long long)B * H > 49152) ||
+        topk > 16 || topk > V)
         return fail(MEDUSA_ERR_UNSUPPORTED,
-                    "heads_topk: unsupported shape (B=%d K=%d H=%d V=%d topk=%d): need B<=8, K<=64, "
-                    "8<=H<=16384, H%%8==0, B*H<=49152, topk<=16, topk<=V",
+                    "heads_topk: unsupported shape (B=%d K=%d H=%d V=%d topk=%d): need K<=64, "
+                    "8<=H<=16384, H%%8==0, topk<=16, topk<=V, and B<=8 with B*H<=49152, or B<=64 "
+                    "for bf16 with H%%128==0",
                     B, K, H, V, topk);
     return MEDUSA_OK;
 }
@@ -458,6 +465,8 @@ extern "C" int medusa_heads_topk(const void* h, const void* w1, const void* b1, 
         return fail(MEDUSA_ERR_INVALID_ARG, "heads_topk: w1 and w2 must be 16-byte aligned");
     if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
         return fail(MEDUSA_ERR_UNSUPPORTED, "heads_topk: unknown dtype %d", (int)dtype);
+    if (B > 8 && dtype != MEDUSA_BF16)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "heads_topk: batches above 8 need bf16 (batch %d)", B);
     HeadsPlan p = plan_heads(B, K, H, V, topk);
     if (!ws || ws_bytes < p.ws_bytes)
         return fail(MEDUSA_ERR_WORKSPACE, "heads_topk: workspace of %zu bytes needed, %zu given",
@@ -537,8 +546,10 @@ extern "C" int medusa_heads_topk_static(const void* h, const void* w1, const voi
     void* ws = nullptr;
     rc = static_scratch(&ws);
     if (rc) return rc;
-    // No scratch byte needs to start at zero: the call writes every byte it
-    // reads (z before the vocab pass, the slice lists before the merge).
+    // No scratch byte needs to start at zero: the call writes every byte whose
+    // value it uses (z before the vocab pass, the slice lists before the merge;
+    // the padding rows of the z planes at batches above 8 are loaded but feed
+    // only accumulator columns that are never read).
     return medusa_heads_topk(h, w1, b1, w2, dtype, B, K, H, V, topk, topk_idx, topk_val, logits, ws,
                              (size_t)MEDUSA_HEADS_STATIC_SCRATCH_BYTES, stream);
 }

@@ -87,7 +87,9 @@ def test_host_side_argument_errors(M):
                              None, 0, None)
     assert rc == -1 and b"null" in L.medusa_last_error()
     # unsupported shapes
-    assert L.medusa_heads_topk(None, None, None, None, 1, 9, 5, 4096, 32000, 8, None, None, None,
+    assert L.medusa_heads_topk(None, None, None, None, 1, 65, 5, 4096, 32000, 8, None, None, None,
+                               None, 0, None) == -2
+    assert L.medusa_heads_topk(None, None, None, None, 0, 9, 5, 4096, 32000, 8, None, None, None,
                                None, 0, None) == -2
     assert L.medusa_heads_topk(None, None, None, None, 1, 1, 5, 4095, 32000, 8, None, None, None,
                                None, 0, None) == -2

@@ -30,6 +30,14 @@ def _run(M, x, topk):
     (5, 384, 1337, 4, 8, "bf16", 2e-2),
     (6, 640, 4099, 5, 8, "bf16", 2e-2),
     (7, 128, 300, 6, 4, "bf16", 2e-2),
+    # batches 9-64 (bf16, H % 128 == 0): padded to a multiple of 16, planes at
+    # columns [0, Bp), [Bp, 2Bp), [2Bp, 3Bp), running per-sequence lists
+    (9, 256, 1000, 3, 8, "bf16", 2e-2),
+    (16, 384, 1337, 4, 8, "bf16", 2e-2),
+    (20, 512, 3001, 5, 16, "bf16", 2e-2),
+    (33, 128, 300, 2, 4, "bf16", 2e-2),
+    (48, 256, 777, 3, 8, "bf16", 2e-2),
+    (64, 256, 1000, 5, 8, "bf16", 2e-2),
 ])
 def test_heads_small(medusa, B, H, V, K, topk, dtype, tol):
     x = W.heads_inputs(seed=B * 7 + K, B=B, H=H, V=V, K=K, dtype=dtype, b1_std=0.5)
@@ -64,6 +72,27 @@ def test_heads_full_size(medusa, cfg, sample):
     assert np.abs(lg[rows] - ref).max() <= 2e-2
     ridx, _ = O.topk(ref, c["topk"])
     topk_near_tie_ok(idx[rows], ridx, ref)
+
+
+def test_heads_batch64_full_size(medusa):
+    # Vicuna-7B-shaped heads at batch 64 (the top of the batch sweep); the oracle
+    # checks three sequences
+    x = W.heads_inputs(seed=64, B=64, H=4096, V=32000, K=5, dtype="bf16")
+    idx, val, lg = _run(medusa, x, 8)
+    rows = [0, 31, 63]
+    ref = O.heads_logits(x["h"][rows], x["w1"], x["b1"], x["w2"], "bf16")
+    assert np.abs(lg[rows] - ref).max() <= 2e-2
+    ridx, _ = O.topk(ref, 8)
+    topk_near_tie_ok(idx[rows], ridx, ref)
+
+
+def test_wide_batch_limits(medusa):
+    # batches above 8 exist only for bf16 with H % 128 == 0, up to 64
+    for B, H, dt in ((9, 256, "f32"), (65, 256, "bf16"), (16, 264, "bf16")):
+        x = W.heads_inputs(seed=5, B=B, H=H, V=300, K=2, dtype=dt)
+        with pytest.raises(medusa.MedusaError) as e:
+            medusa.heads_topk(to_dev(x["h"]), to_dev(x["w1"]), to_dev(x["b1"]), to_dev(x["w2"]), 4)
+        assert e.value.code == -2
 
 
 def test_workspace_and_alignment_errors(medusa):
