@@ -118,7 +118,13 @@ struct AttnSmem {
     // kfull[4] vfull[4] kempty[4] vempty[4] s_full[2] o_done[2] p_full[2] qfull
     static constexpr int kNumBar = 4 * kRing + 7;
     static constexpr int kOffMisc = kOffBar + kNumBar * 8;    // tmem slot, flag
-    static constexpr int kBytes = kOffMisc + 16 + 1024;       // + alignment slack
+    // query blocks of <= 64 rows: a receive area of its own for the split
+    // partials (O [slots][D], then (max, sum) [slots]), so partials can arrive
+    // while this CTA still streams tiles
+    static constexpr int kRecvSlots = 64 + kMaxSplits;
+    static constexpr int kOffRecv = (kOffMisc + 16 + 15) / 16 * 16;
+    static constexpr int kRecvBytes = kRecvSlots * (D + 2) * 4;
+    static constexpr int kBytes = kOffRecv + kRecvBytes + 1024;  // + alignment slack
     // after the tile loop the K/V rings receive the partials of the rows this
     // CTA owns: float O [kMaxSplits][rows_per_owner][D], then (max, sum)
     static constexpr int kOffPartO = kOffK;
@@ -142,20 +148,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
     const int split = blockIdx.x, S = gridDim.x;
     const int hk = blockIdx.y / a.qblocks, qb = blockIdx.y % a.qblocks;
     const int N = a.N, G = a.G;
-    if (threadIdx.x == kTmaWarp * 32 && a.B == 1) {
-        // Warm L2 with this split's first K and V tiles while the previous kernel
-        // finishes.  The rows come from the split's nominal range (no input is
-        // read before the dependency wait); a prefetch is only a hint.
-        const int b = 0;
-        const size_t head = ((size_t)b * a.Hkv + hk) * a.Lmax;
-        for (int t = 0; t < kRing; ++t) {
-            const int key0 = split * a.chunk + t * kBlockN;
-            if (key0 >= a.Lmax) break;
-            const uint32_t bytes = (uint32_t)min(kBlockN, a.Lmax - key0) * D * 2;
-            prefetch_l2_bulk(a.k + (head + key0) * D, bytes);
-            prefetch_l2_bulk(a.v + (head + key0) * D, bytes);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = tid & (kUmmaM - 1), q = (tid >> 7) & 3;
+
+    const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+    uint8_t* base = smem_raw + pad;
+    const uint32_t base_a = smem_addr(base);
+    const uint32_t qs_a = base_a, ks_a = base_a + L::kOffK, vs_a = base_a + L::kOffV;
+    float* red = reinterpret_cast<float*>(base + L::kOffRed);
+    const uint32_t bar_a = base_a + L::kOffBar;
+    const uint32_t kfull0 = bar_a, vfull0 = kfull0 + 8 * kRing, kempty0 = vfull0 + 8 * kRing,
+                   vempty0 = kempty0 + 8 * kRing, s_full0 = vempty0 + 8 * kRing,
+                   o_done0 = s_full0 + 16, p_full0 = o_done0 + 16, qfull = p_full0 + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kOffMisc);
+    volatile int* flag = reinterpret_cast<volatile int*>(base + L::kOffMisc + 4);
+
+    // Set-up that reads no input runs before the dependency wait, overlapping
+    // the previous kernel: barriers, tensor-map prefetch, TMEM, and (batch 1)
+    // an L2 warm-up of this split's K and V rows.
+    if (warp == kTmaWarp && lane == 0) {
+        for (int i = 0; i < L::kNumBar; ++i) mbar_init(bar_a + 8 * i, 1);
+        mbar_init(p_full0, kSoftmaxWarps);
+        mbar_init(p_full0 + 8, kSoftmaxWarps);
+        mbar_init_fence();
+        *flag = 0;
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+        if (a.q_tma) prefetch_tmap(&tmq);
+        if (a.B == 1) {
+            // the rows come from the split's nominal range (no input is read
+            // before the dependency wait); a prefetch is only a hint
+            const size_t head = (size_t)hk * a.Lmax;
+            for (int t = 0; t * kBlockN < a.chunk; ++t) {
+                const int key0 = split * a.chunk + t * kBlockN;
+                if (key0 >= a.Lmax) break;
+                const uint32_t bytes = (uint32_t)min(kBlockN, a.Lmax - key0) * D * 2;
+                prefetch_l2_bulk(a.k + (head + key0) * D, bytes);
+                prefetch_l2_bulk(a.v + (head + key0) * D, bytes);
+            }
         }
     }
+    if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
+    // Blocks of <= 64 query rows merge their split partials through a receive
+    // area of their own: arrive on the cluster barrier now, wait before the
+    // first remote store (which must not precede the peers' start).
+    const bool early_merge = S > 1 && a.spread != 0;
+    if (early_merge) cluster_arrive_relaxed();
     pdl_wait();
     pdl_trigger();
     // Sequences are taken longest first: blockIdx.z is a rank in the order of
@@ -193,32 +231,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
         const int i = spread ? (((m & 31) < 16) ? 16 * (m >> 5) + (m & 15) : -1) : m;
         return (i >= 0 && i < nblk) ? i : -1;
     };
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = tid & (kUmmaM - 1), q = (tid >> 7) & 3;
-
-    const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
-    uint8_t* base = smem_raw + pad;
-    const uint32_t base_a = smem_addr(base);
-    const uint32_t qs_a = base_a, ks_a = base_a + L::kOffK, vs_a = base_a + L::kOffV;
-    float* red = reinterpret_cast<float*>(base + L::kOffRed);
-    const uint32_t bar_a = base_a + L::kOffBar;
-    const uint32_t kfull0 = bar_a, vfull0 = kfull0 + 8 * kRing, kempty0 = vfull0 + 8 * kRing,
-                   vempty0 = kempty0 + 8 * kRing, s_full0 = vempty0 + 8 * kRing,
-                   o_done0 = s_full0 + 16, p_full0 = o_done0 + 16, qfull = p_full0 + 16;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kOffMisc);
-    volatile int* flag = reinterpret_cast<volatile int*>(base + L::kOffMisc + 4);
 
     auto tile_lo = [&](int t) { return k_begin + t * kBlockN; };
     auto tile_start = [&](int t) { return min(k_begin + t * kBlockN, k_end - kBlockN); };
     const int zrow = b * a.Hkv + hk;
 
     if (warp == kTmaWarp && lane == 0) {
-        // barriers first, then the first K/V tiles, while the softmax warps load Q
-        for (int i = 0; i < L::kNumBar; ++i) mbar_init(bar_a + 8 * i, 1);
-        mbar_init(p_full0, kSoftmaxWarps);
-        mbar_init(p_full0 + 8, kSoftmaxWarps);
-        mbar_init_fence();
-        *flag = 0;
+        // Q and the first K/V tiles, while the softmax warps set up
         if (a.q_tma && ntiles > 0) {  // Q rows (node, group member) x D
             if (spread) {  // block rows 16g .. 16g+15 -> TMEM lanes 32g .. 32g+15
                 mbar_expect_tx(qfull, 4 * 16 * D * 2);
@@ -245,7 +264,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
             }
         }
     }
-    if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
     // Q tile without TMA (group size not dividing 128): row rr -> node rr / G,
     // query head hk * G + rr % G; padding rows are zero
     if (!a.q_tma && warp < kSoftmaxWarps) {
@@ -506,12 +524,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
 
     // ------------------ merge the cluster's split partials ------------------
     // row r belongs to CTA r % S and is its (r / S)-th row; split s of it goes to
-    // slot [s][r / S] of the owner's receive area (the owner's rings, free once
-    // every CTA of the cluster has left its tile loop)
-    const int own_rows = (kUmmaM + S - 1) / S;
-    float* part_o = reinterpret_cast<float*>(base + L::kOffPartO);
-    float* part_ml = reinterpret_cast<float*>(base + L::kOffPartML);
-    cluster_sync();
+    // slot [s][r / S] of the owner's receive area.  Blocks of <= 64 rows have a
+    // receive area of their own (the cluster barrier was arrived at before the
+    // tile loop, so its wait here only checks that every peer has started);
+    // larger blocks receive in the owner's rings, free once every CTA of the
+    // cluster has left its tile loop.
+    const int own_rows = early_merge ? (64 + S - 1) / S : (kUmmaM + S - 1) / S;
+    float* part_o = reinterpret_cast<float*>(base + (early_merge ? L::kOffRecv : L::kOffPartO));
+    float* part_ml = early_merge ? part_o + (size_t)L::kRecvSlots * D : reinterpret_cast<float*>(base + L::kOffPartML);
+    if (early_merge) cluster_wait();
+    else cluster_sync();
     if (valid) {
         const int owner = qi % S, slot = split * own_rows + qi / S;
         const uint32_t po = cluster_map(smem_addr(part_o + (size_t)slot * D + q * QW), owner);
