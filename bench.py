@@ -452,17 +452,46 @@ def measure_step_graph(step, layers=32, iters=200, warmup=5):
     torch.cuda.synchronize()
     us = a.elapsed_time(b) * 1e3 / iters
     tokens = float(step.acc["accept_len"].float().mean().item()) + 1.0
+    # the layers' tree attention alone: one graph of `layers` back-to-back
+    # calls, each on its own layer's cache (1.1 GB in all, more than L2, so
+    # every call reads its keys and values from HBM)
+    def att():
+        for l in range(layers):
+            M.tree_attention(step.q, kls[l], vls[l], step.kv_len, step.mask, out=step.att_out, ws=step.ws_att)
+    step.kv_len.copy_(step.kv_len0)
+    with torch.cuda.stream(s):
+        att()
+    torch.cuda.synchronize()
+    ga = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ga, stream=s):
+        att()
+    for _ in range(warmup):
+        ga.replay()
+    torch.cuda.synchronize()
+    reps = max(1, iters // 4)
+    a.record()
+    for _ in range(reps):
+        ga.replay()
+    b.record()
+    torch.cuda.synchronize()
+    us_att = a.elapsed_time(b) * 1e3 / (reps * layers)
+    hbm, _ = _peaks()
+    abytes = algorithmic_bytes(CFG, step.N, int(step.kv_len0.max().item()) + step.N)[1]
     del kc, vc
     return {"layers": layers, "us_per_step": us, "steps_per_s": 1e6 / us, "tokens_per_step": tokens,
-            "tokens_per_s": tokens * 1e6 / us, "launches_per_step": 2 + 1 + layers + 2 + 1}
+            "tokens_per_s": tokens * 1e6 / us, "launches_per_step": 2 + 1 + layers + 2 + 1,
+            "attention_per_layer": {"us": us_att, "algorithmic_bytes": abytes,
+                                    "gbs": abytes / (us_att * 1e-6) / 1e9,
+                                    "frac_hbm": abytes / (us_att * 1e-6) / 1e9 / hbm,
+                                    "method": f"graph of {layers} back-to-back calls, one cache per layer"}}
 
 
 def measure_heads_batches(dev, iters=10, warmup=2):
     """Batch sweep of medusa_heads_topk: hidden 4096 at batch 1, 2, 4, 8, 16, 32
     and 64, and hidden 5120 at batch 8; 5 heads, vocab 32000, top-8, bf16
     (random-init weights of those shapes, allocated once per hidden size; they
-    exceed L2), each point timed over `iters` back-to-back calls.  Batches 1-3
-    run on CUDA cores, 4-64 on the tensor cores."""
+    exceed L2), each point timed over `iters` back-to-back calls.  Batches 1-2
+    run on CUDA cores, 3-64 on the tensor cores."""
     import torch
     import medusa_speculative_decoding_gb300 as M
     hbm, _ = _peaks()
@@ -495,7 +524,7 @@ def measure_heads_batches(dev, iters=10, warmup=2):
             out[f"b{B}_h{H}"] = {"us": us, "gbs": by / (us * 1e-6) / 1e9,
                                  "frac_hbm": by / (us * 1e-6) / 1e9 / hbm, "algorithmic_bytes": by,
                                  "tflops": fl / (us * 1e-6) / 1e12, "sequences_per_s": B * 1e6 / us,
-                                 "path": "tcgen05" if B >= 4 else "cuda cores"}
+                                 "path": "tcgen05" if B >= 3 else "cuda cores"}
             del h, ws
         del w1, b1, w2
     return out

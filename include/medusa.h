@@ -79,7 +79,7 @@ int medusa_abi_version(void);
 /* Limits: 1 <= K <= 64, 8 <= H <= 16384 with H % 8 == 0, topk <= 16,        */
 /* topk <= V, and either 1 <= B <= 8 with B * H <= 49152 (any dtype), or      */
 /* 9 <= B <= 64 for bf16 with H % 128 == 0.  Work is split over the vocab.    */
-/* bf16 batches of 4 to 64 with H % 128 == 0 run on the tensor cores (z is    */
+/* bf16 batches of 3 to 64 with H % 128 == 0 run on the tensor cores (z is    */
 /* carried as three bf16 planes that hold 24 significant bits); h must then   */
 /* be 16-byte aligned.  If a device-side wait gives up there (about one       */
 /* second), the affected topk_idx entries are -1.                             */

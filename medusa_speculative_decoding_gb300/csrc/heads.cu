@@ -3,10 +3,10 @@
 // scores position t + k + 1 through one residual SiLU layer and a vocab
 // projection).
 //
-// At decode batch sizes (B <= 8) both products read weights that are used once
-// per step, so the heads are bound by HBM bandwidth.  bf16 batches of 4 to 8
-// run on the tensor cores (heads_umma.cu); everything else runs here, on CUDA
-// cores, as matrix-vector products:
+// At decode batch sizes both products read weights that are used once per
+// step, so the heads are bound by HBM bandwidth.  bf16 batches of 3 to 64 run
+// on the tensor cores (heads_umma.cu); everything else (batches 1-2, and float32
+// up to batch 8) runs here, on CUDA cores, as matrix-vector products:
 //   K1 heads_w1_silu : z[b,k,:] = h[b] + SiLU(W1_k h[b] + b1_k)   (float32 z);
 //                      the K*H rows of W1 are split evenly over the warps of
 //                      one wave of CTAs
@@ -28,7 +28,7 @@
 
 namespace medusa {
 
-// tensor-core heads for batches of 4 to 8 (heads_umma.cu)
+// tensor-core heads for bf16 batches of 3 to 64 (heads_umma.cu)
 bool heads_umma_applies(int B, int K, int H, int V, int topk, bool bf16);
 size_t heads_umma_workspace(int B, int K, int H, int V, int topk);
 int launch_heads_umma(const void* h, const void* w1, const void* b1, const void* w2, int B, int K, int H,

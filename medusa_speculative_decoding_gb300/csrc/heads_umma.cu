@@ -1,34 +1,30 @@
-// heads_umma.cu -- Medusa heads on the tensor cores for batches of 4 to 64
+// heads_umma.cu -- Medusa heads on the tensor cores for batches of 3 to 64
 // ("Medusa Heads" glossary page, "How heads predict later tokens": head k
 // computes W2_k (h + SiLU(W1_k h + b1_k)) from the last hidden state h).
 //
 // At a batch of one or two the heads are matrix-vector products and stay on
-// CUDA cores (heads.cu).  From a batch of four, every weight element feeds 4-64
-// products and the CUDA-core path runs out of issue slots and shared-memory
+// CUDA cores (heads.cu).  From a batch of three, every weight element feeds
+// 3-64 products and the CUDA-core path runs out of issue slots and shared-memory
 // bandwidth before HBM does, so the same products run as skinny GEMMs on
 // tcgen05: the weights are the M = 128 operand (K-major, streamed by TMA), the
-// batch's vectors the N operand, accumulators in TMEM.
-//   heads_w1_umma_kernel : D[128 W1 rows x N1] = W1 . h^T (h is bf16, exact);
+// batch's vectors the N operand, accumulators in TMEM.  The batch is padded to
+// Bp, a multiple of 16.
+//   heads_w1_umma_kernel : D[128 W1 rows x Bp] = W1 . h^T (h is bf16, exact);
 //                          epilogue z = h + SiLU(D + b1) in float32, written as
 //                          three bf16 planes z = hi + mid + lo (the split keeps
 //                          24 significant bits, as many as float32)
-//   heads_w2_umma_kernel : batches 4-8.  D[128 vocab rows x N] = W2 . [hi; mid;
-//                          lo]^T with N = 3B rounded up to 16; the logit of
-//                          sequence b is the sum of its three columns.  Each CTA
-//                          takes a run of (head, 128-row vocab tile) items, keeps
-//                          every tile's top-k per sequence, reduces each head's
-//                          run to one list, and the last CTA of a head merges the
-//                          head's lists into the final sorted top-k.
-//   heads_w2_umma_wide_kernel : batches 9-64.  The batch is padded to Bp (a
-//                          multiple of 16) and the planes sit at columns [0, Bp),
-//                          [Bp, 2Bp), [2Bp, 3Bp) of an N = 3Bp accumulator.  Each
-//                          sequence keeps a running top-k list of the CTA's run
-//                          in shared memory; a tile only enters the list when one
-//                          of its logits beats the list's last entry.
-// Roles (192 threads): warp 0 TMA producer, warp 1 TMEM allocation and MMA
-// issue, warps 2-5 epilogue (warp w reads TMEM lanes 32*(w%4) ..).  Every wait
-// is bounded; a CTA that gives up marks the call's status word and writes -1
-// into the top-k lists it owns.
+//   heads_w2_umma_kernel : D[128 vocab rows x 3 Bp] = W2 . [hi; mid; lo]^T, the
+//                          planes at columns [0, Bp), [Bp, 2Bp), [2Bp, 3Bp); the
+//                          logit of sequence b is the sum of its three columns.
+//                          Each CTA takes a run of (head, 128-row vocab tile)
+//                          items and keeps every sequence's top-k over its run
+//                          (a tile enters the list only where one of its logits
+//                          beats the list's last entry)
+//   heads_merge_kernel   : merges every head's run lists into the sorted top-k
+// Roles of the two tensor-core kernels (192 threads): warp 0 TMA producer, warp
+// 1 TMEM allocation and MMA issue, warps 2-5 epilogue (warp w reads TMEM lanes
+// 32*(w%4) ..).  Every wait is bounded; a CTA that gives up marks the call's
+// status word, and the merge then writes -1 into every top-k list.
 #include <float.h>
 #include <limits.h>
 
@@ -44,17 +40,10 @@ constexpr int kUM = 128;                 // weight rows per tile (MMA M)
 constexpr int kUK = 64;                  // hidden elements per stage
 constexpr int kUThreads = 192;
 constexpr int kUA = kUM * kUK * 2;       // 16 KB of weight rows per stage
-constexpr int kUBmax = 32 * kUK * 2;     // 4 KB of activation rows per stage (N <= 32)
-constexpr int kUMaxItems = 16;           // W2 items one CTA may own (batches 4-8)
-constexpr int kUMaxB = 8;                // largest batch of the staged W2 kernel
-constexpr int kUMaxBWide = 64;           // largest batch on the tensor cores
+constexpr int kUMinB = 3, kUMaxB = 64;    // batches on the tensor cores
 constexpr int kUTopk = 16;
 constexpr int kUSmemCap = 227 * 1024;    // opt-in shared memory per CTA
 constexpr long long kUWait = 1ll << 31;  // ~1 s at 2 GHz
-// W1: two CTAs per SM (its 160-200 tiles then need no second round); W2: one
-// CTA per SM with a deeper ring, so each SM's share of the 128-row items is
-// within one item of the mean
-constexpr int kW1Stages = 5, kW2Stages = 8;
 
 // ring of STAGES x (16 KB weights + BBYTES activations) | barriers | tmem slot,
 // flags | EXTRA bytes of epilogue staging.  Accumulator buffer i sits at TMEM
@@ -72,64 +61,41 @@ struct UmmaSmem {
     static constexpr int kBytes = kOffExtra + EXTRA + 1024;
     static_assert(kStage % 1024 == 0, "stages start on 1024-byte swizzle atoms");
 };
-// batches 4-8: tile logits float [8][128], then the run staging (values, indices)
-constexpr int kW2Lgt = kUMaxB * kUM * 4;
-constexpr int kW2Run = kUMaxB * kUMaxItems * kUTopk * 4;
-using W1Smem = UmmaSmem<kW1Stages, kUBmax, 32, 64, 0>;
-using W2Smem = UmmaSmem<kW2Stages, kUBmax, 32, 64, kW2Lgt + 2 * kW2Run>;
-// batches 9-64: N1 = Bp <= 64 activation rows, two CTAs per SM
-using W1WideSmem = UmmaSmem<4, kUMaxBWide * kUK * 2, 64, 128, 0>;
+// W1: Bp <= 64 activation rows per stage, two CTAs per SM (the K*H/128 row tiles
+// then need no second round)
+using W1Smem = UmmaSmem<4, kUMaxB * kUK * 2, 64, 128, 0>;
 
-// W2 for batches 9-64 padded to BP: N = 3 BP rows of z planes per stage; tile
-// logits float [BP][129] (rows padded by one word so that threads reading
-// different sequences at the same column hit different banks), and one sorted
-// list of 16 (value, index) pairs per epilogue thread, entry j of thread e at
-// [j][e] (values, then indices)
+// W2 at a batch padded to BP: N = 3 BP rows of z planes per stage (one CTA per
+// SM, as many stages as fit); tile logits float [BP][129] (one padding word per
+// row), and one sorted list of 16 (value, index) pairs per sequence [BP][16]
+// (values, then indices)
 constexpr int kLgtStride = kUM + 1;
 constexpr int kEpi = 128;  // epilogue threads
 template <int BP>
-struct W2Wide {
+struct W2Cfg {
     static constexpr int kN = 3 * BP;
     static constexpr int kBBytes = kN * kUK * 2;
     static constexpr int kLgt = (BP * kLgtStride * 4 + 15) / 16 * 16;
-    static constexpr int kList = kUTopk * kEpi * 8;
+    static constexpr int kList = BP * kUTopk * 8;
     static constexpr int kExtra = kLgt + kList;
     static constexpr int kFit = (kUSmemCap - kExtra - 2048) / (kUA + kBBytes);
     static constexpr int kStages = kFit < 8 ? kFit : 8;
     using Sm = UmmaSmem<kStages, kBBytes, 256, 512, kExtra>;
-    static_assert(BP <= 64 && kN <= 256 && kStages >= 3 && Sm::kBytes <= kUSmemCap, "wide W2 configuration");
+    static_assert(BP <= 64 && kN <= 256 && kStages >= 3 && Sm::kBytes <= kUSmemCap, "W2 configuration");
 };
 
-// Sorted lists of kUTopk (value, index) pairs in shared memory, best first
-// (the order of `better`), one per epilogue thread: entry j of thread e at
-// lv[j * kEpi + e].  Only the first topk entries are ever read out.
-__device__ __forceinline__ void sl_clear(float* lv, int* li, int e) {
-#pragma unroll
-    for (int j = 0; j < kUTopk; ++j) { lv[j * kEpi + e] = -INFINITY; li[j * kEpi + e] = INT_MAX; }
-}
-// inserts (x, xi) at its place, dropping the last entry; returns entry topk - 1
-// (what a new pair must beat from now on) in (tv, ti)
-__device__ __forceinline__ void sl_insert(float* lv, int* li, int e, int topk, float x, int xi, float& tv,
-                                          int& ti) {
-    float cv[kUTopk];
-    int ci[kUTopk];
-#pragma unroll
-    for (int j = 0; j < kUTopk; ++j) { cv[j] = lv[j * kEpi + e]; ci[j] = li[j * kEpi + e]; }
-#pragma unroll
-    for (int j = 0; j < kUTopk; ++j) {
-        if (better(x, xi, cv[j], ci[j])) {
-            const float t0 = cv[j];
-            const int t1 = ci[j];
-            cv[j] = x;
-            ci[j] = xi;
-            x = t0;
-            xi = t1;
-        }
+// One warp keeps a sorted list of kUTopk (value, index) pairs, best first (the
+// order of `better`), as entry j in lane j (lanes from kUTopk on hold empty
+// entries).  Inserting a pair shifts the worse entries down one lane.
+__device__ __forceinline__ void wl_insert(float& ev, int& ei, float cv, int ci, int lane) {
+    const unsigned worse = __ballot_sync(0xffffffffu, better(cv, ci, ev, ei));  // a suffix of lanes
+    const int p = __ffs(worse) - 1;
+    const float uv = __shfl_up_sync(0xffffffffu, ev, 1);
+    const int ui = __shfl_up_sync(0xffffffffu, ei, 1);
+    if (worse != 0u) {
+        if (lane > p) { ev = uv; ei = ui; }
+        else if (lane == p) { ev = cv; ei = ci; }
     }
-#pragma unroll
-    for (int j = 0; j < kUTopk; ++j) { lv[j * kEpi + e] = cv[j]; li[j * kEpi + e] = ci[j]; }
-    tv = lv[(topk - 1) * kEpi + e];
-    ti = li[(topk - 1) * kEpi + e];
 }
 
 // Shared pipeline: warp 0 streams A (weights) and B (activations) slices for
@@ -258,24 +224,21 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
 
 // z = h + SiLU(W1 h + b1) for 128 rows of W1 per item; items are the K*H/128
 // row tiles, dealt evenly over the grid.  N1 activation rows (the batch padded
-// to 16) per MMA; the planes of head k are [3][Bz][H] (Bz = B for batches 4-8,
-// the padded batch above; padding rows are never written and only ever feed
-// accumulator columns that nothing reads).
+// to 16) per MMA; the planes of head k are [3][Bz][H] with Bz the padded batch
+// (padding rows are never written and only ever feed accumulator columns that
+// nothing reads).
 template <typename Sm>
 __global__ void __launch_bounds__(kUThreads, 2) heads_w1_umma_kernel(
     const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmh,
     const uint16_t* __restrict__ h, const uint16_t* __restrict__ b1, int B, int K, int H, int N1, int Bz,
-    uint16_t* __restrict__ zp, unsigned* __restrict__ done, int* __restrict__ status) {
+    uint16_t* __restrict__ zp, int* __restrict__ status) {
     using namespace umma;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint32_t tmem;
     umma_setup<Sm>(base, &tmem);
     pdl_wait();  // h may come from the previous kernel (the last round's compaction)
-    if (blockIdx.x == 0) {
-        for (int k = threadIdx.x; k < K; k += blockDim.x) done[k] = 0u;
-        if (threadIdx.x == 0) *status = 0;
-    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
     pdl_trigger();
     const int tiles = K * H / kUM;
     const int i0 = (int)((long long)blockIdx.x * tiles / gridDim.x);
@@ -318,12 +281,11 @@ __global__ void __launch_bounds__(kUThreads, 2) heads_w1_umma_kernel(
 }
 
 struct W2Args {
-    int B, K, H, V, T, topk, N;
+    int B, K, H, V, T, topk;
     int items;          // K * T
     float* logits;      // [B][K][V] or nullptr
     float* run_val;     // [K][grid][B][topk]
     int* run_idx;
-    unsigned* done;     // [K]
     int* status;
     int32_t* topk_idx;  // [B][K][topk]
     float* topk_val;    // or nullptr
@@ -342,149 +304,25 @@ __device__ __forceinline__ void head_ctas(int k, int T, int items, int grid, int
     ++c1;
 }
 
-// Called by the four epilogue warps once this CTA's list of head k for every
-// sequence is in run_val / run_idx: counts the CTA in, and the last CTA of the
-// head merges the head's lists into the sorted top-k outputs.
-__device__ __forceinline__ void publish_head(const W2Args& a, int k, int grid, int B, int ew, int lane,
-                                             int* s_last) {
-    using namespace umma;
-    const int topk = a.topk;
-    __threadfence();
-    named_barrier_or(1, 128, false);
-    int h0, h1;
-    head_ctas(k, a.T, a.items, grid, h0, h1);
-    if (ew == 0 && lane == 0) *s_last = atomicAdd(&a.done[k], 1u) == (unsigned)(h1 - h0 - 1);
-    named_barrier_or(1, 128, false);
-    if (!*s_last) return;
-    __threadfence();
-    const int m = (h1 - h0) * topk;
-    for (int b = ew; b < B; b += 4) {
-        int32_t* oi = a.topk_idx + ((size_t)b * a.K + k) * topk;
-        float* ov = a.topk_val ? a.topk_val + ((size_t)b * a.K + k) * topk : nullptr;
-        warp_merge_topk<kUTopk>(
-            m, topk,
-            [&](int j, float& x, int& xi) {
-                const int cc = h0 + j / topk, e = j - (j / topk) * topk;
-                const size_t o = (((size_t)k * grid + cc) * B + b) * topk + e;
-                x = __ldcg(a.run_val + o);
-                xi = __ldcg(a.run_idx + o);
-            },
-            [&](int t, float v, int i) {
-                oi[t] = i;
-                if (ov) ov[t] = v;
-            },
-            lane);
-    }
-}
-
-template <int NB>
+// The batch padded to BP.  Epilogue warp w owns sequences w, w + 4, ..:
+// it keeps each one's sorted top-k over the items of the CTA's current head run
+// as a list in shared memory.  Per item the warp tests the sequence's 128
+// logits against the list's entry topk - 1 (four compares per lane and a
+// ballot); the few that beat it are inserted one by one with lane shuffles, and
+// only when many do (a run's first item) is the list rebuilt by a warp
+// selection over list and tile.  At the end of a run the lists are published to
+// run_val / run_idx; heads_merge_kernel then merges every head's run lists.
+template <int BP>
 __global__ void __launch_bounds__(kUThreads, 1) heads_w2_umma_kernel(
     const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmz, W2Args a) {
     using namespace umma;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    float* lgt = reinterpret_cast<float*>(base + W2Smem::kOffExtra);
-    float* runv = reinterpret_cast<float*>(base + W2Smem::kOffExtra + kW2Lgt);
-    int* runi = reinterpret_cast<int*>(base + W2Smem::kOffExtra + kW2Lgt + kW2Run);
-    __shared__ int s_last;
-    uint32_t tmem;
-    umma_setup<W2Smem>(base, &tmem);
-    pdl_wait();  // the z planes come from heads_w1_umma_kernel
-    pdl_trigger();
-    const int c = blockIdx.x, grid = gridDim.x;
-    const int i0 = (int)((long long)c * a.items / grid), i1 = (int)((long long)(c + 1) * a.items / grid);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3;
-    constexpr int B = NB;
-    const int T = a.T, topk = a.topk;
-    const int ew = warp - 2;  // epilogue warp 0..3
-    auto coords = [&](int it, int& ay, int& by) {
-        const int g = i0 + it, k = g / T, t = g - k * T;
-        ay = k * a.V + t * kUM;
-        by = k * 3 * B;
-    };
-    // Writes head k's run (items [r0, r1) of this CTA, staged in runv/runi) as
-    // one top-k list per sequence, then merges the head if this CTA is last.
-    auto finish_run = [&](int k, int nstaged) {
-        for (int b = ew; b < B; b += 4) {
-            float* ov = a.run_val + (((size_t)k * grid + c) * B + b) * topk;
-            int* oi = a.run_idx + (((size_t)k * grid + c) * B + b) * topk;
-            const float* sv = runv + b * kUMaxItems * kUTopk;
-            const int* si = runi + b * kUMaxItems * kUTopk;
-            warp_select_topk(
-                nstaged, topk, [&](int j, float& x, int& xi) { x = sv[j]; xi = si[j]; },
-                [&](int t, float v, int i) { ov[t] = v; oi[t] = i; }, lane);
-        }
-        publish_head(a, k, grid, B, ew, lane, &s_last);
-    };
-    int run_k = -1, nstaged = 0;
-    auto epi = [&](int it, uint32_t col) {
-        const int g = i0 + it, k = g / T, t = g - k * T;
-        if (k != run_k) {
-            if (run_k >= 0) finish_run(run_k, nstaged);
-            run_k = k;
-            nstaged = 0;
-        }
-        const int vl = q * 32 + lane, v = t * kUM + vl;
-        float d[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + col, d);
-        tmem_wait_ld();
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-            const float x = v < a.V ? d[b] + d[B + b] + d[2 * B + b] : -INFINITY;
-            lgt[b * kUM + vl] = x;
-            if (a.logits && v < a.V) a.logits[((size_t)b * a.K + k) * a.V + v] = x;
-        }
-        named_barrier_or(1, 128, false);
-        for (int b = ew; b < B; b += 4) {
-            float* sv = runv + b * kUMaxItems * kUTopk + nstaged;
-            int* si = runi + b * kUMaxItems * kUTopk + nstaged;
-            const float* row = lgt + b * kUM;
-            warp_select_topk(
-                kUM, topk, [&](int j, float& x, int& xi) { x = row[j]; xi = t * kUM + j; },
-                [&](int tt, float vv, int ii) { sv[tt] = vv; si[tt] = ii; }, lane);
-        }
-        nstaged += topk;
-        named_barrier_or(1, 128, false);
-    };
-    // a failure of the first kernel leaves the z planes undefined
-    const bool ok1 = __syncthreads_or(*(volatile int*)a.status != 0) == 0;
-    bool ok = ok1 && umma_pipeline<W2Smem>(base, tmem, i1 - i0, a.H / kUK, a.N, &tmw, &tmz, coords, epi);
-    if (ok && warp >= 2 && run_k >= 0) finish_run(run_k, nstaged);
-    if (!ok) {
-        // every list of the heads this CTA touches is marked invalid
-        if (threadIdx.x == 0) atomicExch(a.status, 1);
-        const int k0 = i0 / T, k1 = (i1 - 1) / T;
-        const int n = (k1 - k0 + 1) * B * topk;
-        for (int j = threadIdx.x; j < n; j += blockDim.x) {
-            const int e = j % topk, b = (j / topk) % B, k = k0 + j / (topk * B);
-            a.topk_idx[((size_t)b * a.K + k) * topk + e] = -1;
-        }
-    }
-    if (warp == 1) {
-        umma::fence_after_sync();
-        umma::tmem_dealloc(tmem, W2Smem::kTmemCols);
-    }
-}
-
-// Batches 9-64, padded to BP.  The 128 epilogue threads own (sequence, half
-// tile) pairs: thread e keeps the sorted top-k of sequence e % 64 over the tile
-// rows [64 (e / 64), 64 (e / 64) + 64) of every item of the CTA's current head
-// run.  A logit costs one shared-memory load and one compare against the list's
-// last entry (kept in registers); it is inserted only when it beats it (after
-// the first few tiles of a run that is rare).  At the end of a run the two half
-// lists of a sequence are merged into the run's list in run_val / run_idx;
-// heads_merge_kernel then merges every head's run lists.
-template <int BP>
-__global__ void __launch_bounds__(kUThreads, 1) heads_w2_umma_wide_kernel(
-    const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmz, W2Args a) {
-    using namespace umma;
-    using Cfg = W2Wide<BP>;
+    using Cfg = W2Cfg<BP>;
     using Sm = typename Cfg::Sm;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     float* lgt = reinterpret_cast<float*>(base + Sm::kOffExtra);               // [BP][129]
-    float* lvs = reinterpret_cast<float*>(base + Sm::kOffExtra + Cfg::kLgt);  // [16][128]
-    int* lis = reinterpret_cast<int*>(lvs + kUTopk * kEpi);
+    float* lvs = reinterpret_cast<float*>(base + Sm::kOffExtra + Cfg::kLgt);  // [BP][16]
+    int* lis = reinterpret_cast<int*>(lvs + BP * kUTopk);
     uint32_t tmem;
     umma_setup<Sm>(base, &tmem);
     pdl_wait();  // the z planes come from heads_w1_umma_kernel
@@ -493,39 +331,30 @@ __global__ void __launch_bounds__(kUThreads, 1) heads_w2_umma_wide_kernel(
     const int i0 = (int)((long long)c * a.items / grid), i1 = (int)((long long)(c + 1) * a.items / grid);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3;
     const int B = a.B, T = a.T, topk = a.topk;
-    const int e = (warp - 2) * 32 + lane;    // epilogue thread 0..127 (warps 2-5)
-    const int sb = e & 63, half = e >> 6;    // its sequence and half tile
-    const bool sel = warp >= 2 && sb < B;
+    const int ew = warp - 2;  // epilogue warp 0..3
     auto coords = [&](int it, int& ay, int& by) {
         const int g = i0 + it, k = g / T, t = g - k * T;
         ay = k * a.V + t * kUM;
         by = k * 3 * BP;
     };
-    float tv = -INFINITY;  // entry topk - 1 of this thread's list
-    int ti = INT_MAX;
-    if (warp >= 2) sl_clear(lvs, lis, e);
-    // head k's run is complete: merge each sequence's two half lists into the
-    // run's list and publish it
+    auto clear_lists = [&]() {
+        for (int sq = ew; sq < B; sq += 4)
+            if (lane < kUTopk) { lvs[sq * kUTopk + lane] = -INFINITY; lis[sq * kUTopk + lane] = INT_MAX; }
+        __syncwarp();
+    };
+    // head k's run is complete: publish every sequence's list, clear the lists
     auto finish_run = [&](int k) {
-        named_barrier_or(1, kEpi, false);  // every half list is complete
-        if (sel && half == 0) {
-            const size_t o = (((size_t)k * grid + c) * B + sb) * topk;
-            int p0 = 0, p1 = 0;
-            for (int t = 0; t < topk; ++t) {
-                const float v0 = lvs[p0 * kEpi + e], v1 = lvs[p1 * kEpi + e + 64];
-                const int x0 = lis[p0 * kEpi + e], x1 = lis[p1 * kEpi + e + 64];
-                const bool first = better(v0, x0, v1, x1);
-                a.run_val[o + t] = first ? v0 : v1;
-                a.run_idx[o + t] = first ? x0 : x1;
-                p0 += first ? 1 : 0;
-                p1 += first ? 0 : 1;
+        for (int sq = ew; sq < B; sq += 4) {
+            if (lane < topk) {
+                const size_t o = (((size_t)k * grid + c) * B + sq) * topk + lane;
+                a.run_val[o] = lvs[sq * kUTopk + lane];
+                a.run_idx[o] = lis[sq * kUTopk + lane];
             }
         }
-        named_barrier_or(1, kEpi, false);
-        sl_clear(lvs, lis, e);
-        tv = -INFINITY;
-        ti = INT_MAX;
+        __syncwarp();
+        clear_lists();
     };
+    if (warp >= 2) clear_lists();
     int run_k = -1;
     auto epi = [&](int it, uint32_t col) {
         const int g = i0 + it, k = g / T, t = g - k * T;
@@ -552,14 +381,65 @@ __global__ void __launch_bounds__(kUThreads, 1) heads_w2_umma_wide_kernel(
             }
         }
         named_barrier_or(1, kEpi, false);
-        if (sel) {
-            const float* row = lgt + sb * kLgtStride + half * 64;
-            const int idx0 = t * kUM + half * 64;
-#pragma unroll 8
-            for (int j = 0; j < 64; ++j) {
-                const float x = row[j];
-                if (better(x, idx0 + j, tv, ti)) sl_insert(lvs, lis, e, topk, x, idx0 + j, tv, ti);
+        for (int sq = ew; sq < B; sq += 4) {
+            const float* row = lgt + sq * kLgtStride;
+            float* Lv = lvs + sq * kUTopk;
+            int* Li = lis + sq * kUTopk;
+            float ev = lane < kUTopk ? Lv[lane] : -INFINITY;
+            int ei = lane < kUTopk ? Li[lane] : INT_MAX;
+            float tv = __shfl_sync(0xffffffffu, ev, topk - 1);
+            int ti = __shfl_sync(0xffffffffu, ei, topk - 1);
+            float x[kUM / 32];
+            unsigned m = 0;
+#pragma unroll
+            for (int u = 0; u < kUM / 32; ++u) {
+                x[u] = row[lane + 32 * u];
+                if (better(x[u], t * kUM + lane + 32 * u, tv, ti)) m |= 1u << u;
             }
+            const int ncand = __reduce_add_sync(0xffffffffu, __popc(m));
+            if (ncand == 0) continue;
+            if (ncand > 2 * kUTopk) {
+                // many candidates: rebuild the list by selection over list and tile
+                float lastv = INFINITY;
+                int lasti = -1;
+                for (int tt = 0; tt < topk; ++tt) {
+                    float bv = -INFINITY;
+                    int bi = INT_MAX;
+                    for (int j = lane; j < kUTopk + kUM; j += 32) {
+                        const float xv = j < kUTopk ? Lv[j] : row[j - kUTopk];
+                        const int xi = j < kUTopk ? Li[j] : t * kUM + (j - kUTopk);
+                        if (better(lastv, lasti, xv, xi) && better(xv, xi, bv, bi)) { bv = xv; bi = xi; }
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+                    }
+                    if (lane == tt) { ev = bv; ei = bi; }
+                    lastv = bv;
+                    lasti = bi;
+                }
+                if (lane >= topk) { ev = -INFINITY; ei = INT_MAX; }
+            } else {
+#pragma unroll
+                for (int u = 0; u < kUM / 32; ++u) {
+                    unsigned bal = __ballot_sync(0xffffffffu, (m >> u) & 1u);
+                    while (bal) {
+                        const int src = __ffs(bal) - 1;
+                        bal &= bal - 1;
+                        const float cv = __shfl_sync(0xffffffffu, x[u], src);
+                        const int ci = t * kUM + src + 32 * u;
+                        if (!better(cv, ci, tv, ti)) continue;  // the list moved on meanwhile
+                        wl_insert(ev, ei, cv, ci, lane);
+                        tv = __shfl_sync(0xffffffffu, ev, topk - 1);
+                        ti = __shfl_sync(0xffffffffu, ei, topk - 1);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane < kUTopk) { Lv[lane] = ev; Li[lane] = ei; }
+            __syncwarp();
         }
         named_barrier_or(1, kEpi, false);
     };
@@ -582,11 +462,11 @@ __global__ void __launch_bounds__(kUThreads, 1) heads_w2_umma_wide_kernel(
     }
 }
 
-// Batches 9-64: one warp per (head, sequence) merges the run lists of the CTAs
+// One warp per (head, sequence) merges the run lists of the CTAs
 // whose items met the head (grid2 = the W2 kernel's grid) into the sorted
 // top-k.  If an earlier kernel of the call gave up a wait, every list is -1.
 __global__ void __launch_bounds__(128) heads_merge_kernel(W2Args a, int grid2) {
-    pdl_wait();  // the run lists come from heads_w2_umma_wide_kernel
+    pdl_wait();  // the run lists come from heads_w2_umma_kernel
     pdl_trigger();
     const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (w >= a.K * a.B) return;
@@ -636,44 +516,36 @@ int bf16_rows_map(CUtensorMap* m, const void* p, int H, long long rows, int box_
 // W2 items are dealt over one CTA per SM
 int umma_grid() { return sm_count(); }
 
-// batch padded to a multiple of 16 for batches 9-64 (the wide kernels)
-static int wide_pad(int B) { return (B + 15) / 16 * 16; }
-// rows of z planes per head: B for batches 4-8, the padded batch above
-static int plane_rows(int B) { return B <= kUMaxB ? B : wide_pad(B); }
+// the batch padded to a multiple of 16
+static int pad16(int B) { return (B + 15) / 16 * 16; }
 
-static int wide_w2_smem(int Bp) {
+static int w2_smem(int Bp) {
     switch (Bp) {
-        case 16: return W2Wide<16>::Sm::kBytes;
-        case 32: return W2Wide<32>::Sm::kBytes;
-        case 48: return W2Wide<48>::Sm::kBytes;
-        default: return W2Wide<64>::Sm::kBytes;
+        case 16: return W2Cfg<16>::Sm::kBytes;
+        case 32: return W2Cfg<32>::Sm::kBytes;
+        case 48: return W2Cfg<48>::Sm::kBytes;
+        default: return W2Cfg<64>::Sm::kBytes;
     }
 }
 
 bool heads_umma_applies(int B, int K, int H, int V, int topk, bool bf16) {
-    const int grid = umma_grid();
-    const int T = (V + kUM - 1) / kUM;
-    if (!bf16 || B < 4 || B > kUMaxBWide || H % kUM != 0 || topk > kUTopk || (long long)K * V >= (1ll << 31))
-        return false;
-    if (B <= kUMaxB)
-        return ((long long)K * T + grid - 1) / grid <= kUMaxItems && W2Smem::kBytes <= max_smem_optin();
-    return wide_w2_smem(wide_pad(B)) <= max_smem_optin() && W1WideSmem::kBytes <= max_smem_optin();
+    return bf16 && B >= kUMinB && B <= kUMaxB && H % kUM == 0 && topk <= kUTopk &&
+           (long long)K * V < (1ll << 31) && w2_smem(pad16(B)) <= max_smem_optin() &&
+           W1Smem::kBytes <= max_smem_optin();
 }
 
 size_t heads_umma_workspace(int B, int K, int H, int V, int topk) {
     const int grid = umma_grid();
-    size_t off = align_up((size_t)K * 3 * plane_rows(B) * H * 2, 256);    // z planes
+    size_t off = align_up((size_t)K * 3 * pad16(B) * H * 2, 256);      // z planes
     off = align_up(off + (size_t)K * grid * B * topk * 4, 256);            // run values
     off = align_up(off + (size_t)K * grid * B * topk * 4, 256);            // run indices
-    off = align_up(off + (size_t)K * 4, 256);                              // done counters
     return align_up(off + 16, 256);                                        // status
 }
 
 template <int BP>
-cudaError_t launch_w2_wide(const CUtensorMap& tw2, const CUtensorMap& tz, const W2Args& a, int grid,
-                           cudaStream_t st) {
-    auto k2 = heads_w2_umma_wide_kernel<BP>;
-    constexpr int smem = W2Wide<BP>::Sm::kBytes;
+cudaError_t launch_w2(const CUtensorMap& tw2, const CUtensorMap& tz, const W2Args& a, int grid, cudaStream_t st) {
+    auto k2 = heads_w2_umma_kernel<BP>;
+    constexpr int smem = W2Cfg<BP>::Sm::kBytes;
     cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     return launch(k2, dim3(grid), dim3(kUThreads), (size_t)smem, st, tw2, tz, a);
 }
@@ -683,70 +555,44 @@ int launch_heads_umma(const void* h, const void* w1, const void* b1, const void*
                       cudaStream_t st) {
     const int grid = umma_grid();
     const int T = (V + kUM - 1) / kUM;
-    const bool wide = B > kUMaxB;
-    const int Bz = plane_rows(B);                              // z plane rows per head
-    const int N1 = wide ? Bz : 16;                             // W1 MMA N (h rows, padded)
-    const int N = wide ? 3 * Bz : (3 * B + 15) / 16 * 16;      // W2 MMA N
+    const int Bp = pad16(B);  // z plane rows per head, and the W1 MMA's N
     uint16_t* zp = reinterpret_cast<uint16_t*>(ws);
-    size_t off = align_up((size_t)K * 3 * Bz * H * 2, 256);
+    size_t off = align_up((size_t)K * 3 * Bp * H * 2, 256);
     float* run_val = reinterpret_cast<float*>(ws + off);
     off = align_up(off + (size_t)K * grid * B * topk * 4, 256);
     int* run_idx = reinterpret_cast<int*>(ws + off);
     off = align_up(off + (size_t)K * grid * B * topk * 4, 256);
-    unsigned* done = reinterpret_cast<unsigned*>(ws + off);
-    off = align_up(off + (size_t)K * 4, 256);
     int* status = reinterpret_cast<int*>(ws + off);
     CUtensorMap tw1, th, tw2, tz;
     int rc = bf16_rows_map(&tw1, w1, H, (long long)K * H, kUM);
-    if (!rc) rc = bf16_rows_map(&th, h, H, B, N1);
+    if (!rc) rc = bf16_rows_map(&th, h, H, B, Bp);
     if (!rc) rc = bf16_rows_map(&tw2, w2, H, (long long)K * V, kUM);
-    if (!rc) rc = bf16_rows_map(&tz, zp, H, (long long)K * 3 * Bz, N);
+    if (!rc) rc = bf16_rows_map(&tz, zp, H, (long long)K * 3 * Bp, 3 * Bp);
     if (rc) return rc;
     const int tiles1 = K * H / kUM;
-    cudaError_t e;
-    if (wide) {
-        auto k1 = heads_w1_umma_kernel<W1WideSmem>;
-        cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, W1WideSmem::kBytes);
-        e = launch(k1, dim3(min(2 * grid, tiles1)), dim3(kUThreads), (size_t)W1WideSmem::kBytes, st, tw1, th,
-                   static_cast<const uint16_t*>(h), static_cast<const uint16_t*>(b1), B, K, H, N1, Bz, zp, done,
-                   status);
-    } else {
-        auto k1 = heads_w1_umma_kernel<W1Smem>;
-        cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, W1Smem::kBytes);
-        e = launch(k1, dim3(min(2 * grid, tiles1)), dim3(kUThreads), (size_t)W1Smem::kBytes, st, tw1, th,
-                   static_cast<const uint16_t*>(h), static_cast<const uint16_t*>(b1), B, K, H, N1, Bz, zp, done,
-                   status);
-    }
+    auto k1 = heads_w1_umma_kernel<W1Smem>;
+    cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, W1Smem::kBytes);
+    cudaError_t e = launch(k1, dim3(min(2 * grid, tiles1)), dim3(kUThreads), (size_t)W1Smem::kBytes, st, tw1, th,
+                           static_cast<const uint16_t*>(h), static_cast<const uint16_t*>(b1), B, K, H, Bp, Bp, zp,
+                           status);
     if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "heads_w1_umma: launch failed: %s", cudaGetErrorString(e));
     W2Args a{};
-    a.B = B; a.K = K; a.H = H; a.V = V; a.T = T; a.topk = topk; a.N = N;
+    a.B = B; a.K = K; a.H = H; a.V = V; a.T = T; a.topk = topk;
     a.items = K * T;
     a.logits = logits;
     a.run_val = run_val;
     a.run_idx = run_idx;
-    a.done = done;
     a.status = status;
     a.topk_idx = topk_idx;
     a.topk_val = topk_val;
     const int g2 = min(grid, a.items);
-    if (wide) {
-        e = Bz == 16 ? launch_w2_wide<16>(tw2, tz, a, g2, st)
-          : Bz == 32 ? launch_w2_wide<32>(tw2, tz, a, g2, st)
-          : Bz == 48 ? launch_w2_wide<48>(tw2, tz, a, g2, st)
-                     : launch_w2_wide<64>(tw2, tz, a, g2, st);
-        if (e != cudaSuccess)
-            return fail(MEDUSA_ERR_CUDA, "heads_w2_umma: launch failed: %s", cudaGetErrorString(e));
-        e = launch(heads_merge_kernel, dim3((K * B + 3) / 4), dim3(128), 0, st, a, g2);
-        if (e != cudaSuccess)
-            return fail(MEDUSA_ERR_CUDA, "heads_merge: launch failed: %s", cudaGetErrorString(e));
-        return MEDUSA_OK;
-    } else {
-        auto k2 = B == 4 ? heads_w2_umma_kernel<4> : B == 5 ? heads_w2_umma_kernel<5>
-                : B == 6 ? heads_w2_umma_kernel<6> : B == 7 ? heads_w2_umma_kernel<7> : heads_w2_umma_kernel<8>;
-        cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, W2Smem::kBytes);
-        e = launch(k2, dim3(g2), dim3(kUThreads), (size_t)W2Smem::kBytes, st, tw2, tz, a);
-    }
+    e = Bp == 16 ? launch_w2<16>(tw2, tz, a, g2, st)
+      : Bp == 32 ? launch_w2<32>(tw2, tz, a, g2, st)
+      : Bp == 48 ? launch_w2<48>(tw2, tz, a, g2, st)
+                 : launch_w2<64>(tw2, tz, a, g2, st);
     if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "heads_w2_umma: launch failed: %s", cudaGetErrorString(e));
+    e = launch(heads_merge_kernel, dim3((K * B + 3) / 4), dim3(128), 0, st, a, g2);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "heads_merge: launch failed: %s", cudaGetErrorString(e));
     return MEDUSA_OK;
 }
 
