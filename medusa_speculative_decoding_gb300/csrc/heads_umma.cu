@@ -70,7 +70,8 @@ using W1Smem = UmmaSmem<4, kUMaxB * kUK * 2, 64, 128, 0>;
 // row), and one sorted list of 16 (value, index) pairs per sequence [BP][16]
 // (values, then indices)
 constexpr int kLgtStride = kUM + 1;
-constexpr int kEpi = 128;  // epilogue threads
+constexpr int kEpi = 128;      // epilogue threads
+constexpr int kRebuildAt = 6;  // more candidates than this: rebuild instead of inserting
 template <int BP>
 struct W2Cfg {
     static constexpr int kN = 3 * BP;
@@ -308,9 +309,9 @@ __device__ __forceinline__ void head_ctas(int k, int T, int items, int grid, int
 // it keeps each one's sorted top-k over the items of the CTA's current head run
 // as a list in shared memory.  Per item the warp tests the sequence's 128
 // logits against the list's entry topk - 1 (four compares per lane and a
-// ballot); the few that beat it are inserted one by one with lane shuffles, and
-// only when many do (a run's first item) is the list rebuilt by a warp
-// selection over list and tile.  At the end of a run the lists are published to
+// ballot); a few that beat it are inserted one by one with lane shuffles, and
+// when more do (always on a run's first item) the list is rebuilt from list and
+// tile by passes that pop the best of the lanes' sorted registers.  At the end of a run the lists are published to
 // run_val / run_idx; heads_merge_kernel then merges every head's run lists.
 template <int BP>
 __global__ void __launch_bounds__(kUThreads, 1) heads_w2_umma_kernel(
@@ -398,29 +399,50 @@ __global__ void __launch_bounds__(kUThreads, 1) heads_w2_umma_kernel(
             }
             const int ncand = __reduce_add_sync(0xffffffffu, __popc(m));
             if (ncand == 0) continue;
-            if (ncand > 2 * kUTopk) {
-                // many candidates: rebuild the list by selection over list and tile
-                float lastv = INFINITY;
-                int lasti = -1;
+            if (ncand > kRebuildAt) {
+                // many candidates: rebuild the list from list and tile.  Each
+                // lane sorts its four tile logits and its list entry; each pass
+                // takes the best head across the warp into lane `tt` and the
+                // lane that held it pops it.
+                float cv[kUM / 32 + 1];
+                int ci[kUM / 32 + 1];
+#pragma unroll
+                for (int u = 0; u < kUM / 32; ++u) { cv[u] = x[u]; ci[u] = t * kUM + lane + 32 * u; }
+                cv[kUM / 32] = ev;
+                ci[kUM / 32] = ei;
+#pragma unroll
+                for (int i = 1; i <= kUM / 32; ++i)
+#pragma unroll
+                    for (int j = i; j > 0; --j)
+                        if (better(cv[j], ci[j], cv[j - 1], ci[j - 1])) {
+                            const float tv0 = cv[j];
+                            const int ti0 = ci[j];
+                            cv[j] = cv[j - 1];
+                            ci[j] = ci[j - 1];
+                            cv[j - 1] = tv0;
+                            ci[j - 1] = ti0;
+                        }
+                float nv = -INFINITY;
+                int ni = INT_MAX;
                 for (int tt = 0; tt < topk; ++tt) {
-                    float bv = -INFINITY;
-                    int bi = INT_MAX;
-                    for (int j = lane; j < kUTopk + kUM; j += 32) {
-                        const float xv = j < kUTopk ? Lv[j] : row[j - kUTopk];
-                        const int xi = j < kUTopk ? Li[j] : t * kUM + (j - kUTopk);
-                        if (better(lastv, lasti, xv, xi) && better(xv, xi, bv, bi)) { bv = xv; bi = xi; }
-                    }
+                    float bv = cv[0];
+                    int bi = ci[0];
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) {
                         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
                         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
                         if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
                     }
-                    if (lane == tt) { ev = bv; ei = bi; }
-                    lastv = bv;
-                    lasti = bi;
+                    if (lane == tt) { nv = bv; ni = bi; }
+                    if (cv[0] == bv && ci[0] == bi) {
+#pragma unroll
+                        for (int e = 0; e < kUM / 32; ++e) { cv[e] = cv[e + 1]; ci[e] = ci[e + 1]; }
+                        cv[kUM / 32] = -INFINITY;
+                        ci[kUM / 32] = INT_MAX;
+                    }
                 }
-                if (lane >= topk) { ev = -INFINITY; ei = INT_MAX; }
+                ev = nv;
+                ei = ni;
             } else {
 #pragma unroll
                 for (int u = 0; u < kUM / 32; ++u) {
