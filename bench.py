@@ -654,6 +654,31 @@ def replica_throughput(steps, ms_total, world):
     return world * steps / (ms_total / 1e3)
 
 
+def only_heads(B, H, calls):
+    """medusa_heads_topk alone at batch B, `calls` back-to-back calls (a short
+    command for ncu captures of the heads kernels at one batch size)."""
+    import torch
+    import medusa_speculative_decoding_gb300 as M
+    dev = torch.device("cuda", 0)
+    K, V, topk = 5, 32000, 8
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    h = torch.randn(B, H, device=dev, generator=g).bfloat16()
+    w1 = (torch.randn(K, H, H, device=dev, generator=g) * 0.02).bfloat16()
+    b1 = torch.zeros(K, H, device=dev).bfloat16()
+    w2 = (torch.randn(K, V, H, device=dev, generator=g) * 0.02).bfloat16()
+    ws = torch.empty(M.heads_topk_workspace(B, K, H, V, topk), dtype=torch.uint8, device=dev)
+    res = (torch.empty(B, K, topk, dtype=torch.int32, device=dev), torch.empty(B, K, topk, device=dev), None)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(max(1, calls)):
+        a.record()
+        M.heads_topk(h, w1, b1, w2, topk, out=res, ws=ws)
+        b.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"heads_batch": B, "hidden": H, "calls": calls, "last_call_us": a.elapsed_time(b) * 1e3}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -661,9 +686,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-heads", type=int, default=0, metavar="B",
+                    help="profiling aid: run medusa_heads_topk at batch B (hidden --hidden, vocab 32000, "
+                         "5 heads, top-8, bf16, random-init weights) --steps times, print the last "
+                         "call's time, and exit")
+    ap.add_argument("--hidden", type=int, default=4096)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.only_heads:
+        return only_heads(args.only_heads, args.hidden, args.steps)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
