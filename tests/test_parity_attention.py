@@ -22,6 +22,8 @@ def _tree(kind):
         return O.tree_layout(O.product_tree_paths((4, 4, 4, 4)), 4)
     if kind == "small":
         return O.tree_layout(O.sparse_tree_paths(20, 4, 4, 0.6, 0.5), 4)
+    if kind == "max512":  # the largest tree the entry point takes: 512 nodes, 8 mask words
+        return O.tree_layout(O.sparse_tree_paths(512, 8, 8, 0.6, 0.5), 8)
     raise KeyError(kind)
 
 
@@ -39,6 +41,8 @@ def _run(M, x, kv_len, t, scale):
     ("small", 2, 8, 2, 64, [5, 190], 240, "bf16"),
     ("dense", 1, 2, 2, 128, [300], 700, "bf16"),
     ("c1", 4, 4, 4, 64, [1, 63, 64, 65], 80, "bf16"),
+    ("max512", 2, 2, 2, 128, [0, 200], 720, "bf16"),
+    ("max512", 1, 4, 2, 64, [129], 650, "f32"),
 ])
 def test_attention_full_compare(medusa, kind, B, Hq, Hkv, D, lens, Lmax, dtype):
     t = _tree(kind)

@@ -26,6 +26,8 @@ def _run(M, x, topk):
     (3, 264, 3001, 5, 8, "bf16", 2e-2),
     (8, 264, 1000, 3, 8, "bf16", 2e-2),
     (5, 264, 777, 4, 5, "f32", 1e-5),
+    (2, 16384, 300, 1, 4, "bf16", 2e-2),    # largest hidden size (B * H = 32768)
+    (1, 128, 300, 64, 4, "bf16", 2e-2),     # largest head count
     # bf16 batches 3-64 with H % 128 == 0 run on the tensor cores, the batch
     # padded to a multiple of 16 (planes at columns [0, Bp), [Bp, 2Bp),
     # [2Bp, 3Bp)): ragged vocab tiles, heads split across CTAs, runs that cross
@@ -42,6 +44,8 @@ def _run(M, x, topk):
     (33, 128, 300, 2, 4, "bf16", 2e-2),
     (48, 256, 777, 3, 8, "bf16", 2e-2),
     (64, 256, 1000, 5, 8, "bf16", 2e-2),
+    (3, 16384, 300, 1, 4, "bf16", 2e-2),    # largest hidden size on the tensor cores
+    (4, 128, 300, 64, 4, "bf16", 2e-2),     # largest head count on the tensor cores
 ])
 def test_heads_small(medusa, B, H, V, K, topk, dtype, tol):
     x = W.heads_inputs(seed=B * 7 + K, B=B, H=H, V=V, K=K, dtype=dtype, b1_std=0.5)
