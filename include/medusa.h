@@ -166,7 +166,8 @@ int medusa_build_tree(const int32_t* topk_idx, const int32_t* root_tok, const in
 /*   mask    [N, ceil(N/64)] uint64 from medusa_tree_layout                    */
 /*   out     [B,N,Hq,D] float32                                               */
 /* Query head hq reads KV head hq / (Hq / Hkv).  Limits: D in {64, 128},      */
-/* 1 <= N <= 512, Hq % Hkv == 0, N * (Hq/Hkv) <= 4096.                       */
+/* 1 <= N <= 512, Hq % Hkv == 0, N * (Hq/Hkv) <= 4096; scale > 0 and finite   */
+/* (MEDUSA_ERR_INVALID_ARG otherwise).                                        */
 /* The bf16 path merges its KV-split partials on chip and needs no workspace: */
 /* medusa_tree_attention_workspace returns 0 and ws may be NULL.  If a        */
 /* device-side wait gives up (about one second), the affected outputs are NaN. */

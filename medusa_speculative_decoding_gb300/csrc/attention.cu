@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
                 const int c0 = kt + q * SW;  // key of sv[0]
                 if (kt == klo && kt + kBlockN <= min(k_end, Lb)) {  // plain prefix tile
 #pragma unroll
-                    for (int i = 0; i < SW; ++i) { sv[i] *= a.scale_log2; mt = fmaxf(mt, sv[i]); }
+                    for (int i = 0; i < SW; ++i) mt = fmaxf(mt, sv[i]);
                 } else {
                     uint64_t w0 = 0, w1 = 0;
                     int mbase = 0;
@@ -418,10 +418,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
                             const int m = key - Lb - mbase;  // in [0, 96)
                             vis = vis && valid && (((m < 64 ? w0 >> m : w1 >> (m - 64)) & 1ull) != 0);
                         }
-                        sv[i] = vis ? sv[i] * a.scale_log2 : -INFINITY;
+                        sv[i] = vis ? sv[i] : -INFINITY;
                         mt = fmaxf(mt, sv[i]);
                     }
                 }
+                // raw scores are scaled inside the exponent's FMA below; the
+                // scale is positive, so the row maximum scales the same way
+                mt *= a.scale_log2;
             }
             float* rj = red + (j & 1) * 4 * 128;
             rj[q * 128 + r] = mt;
@@ -469,10 +472,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
                 float psum = 0.f;
 #pragma unroll
                 for (int e = 0; e < SW / 2; ++e) {
-                    const float p0 = exp2_approx(sv[2 * e] - mr);
-                    const float p1 = exp2_approx(sv[2 * e + 1] - mr);
-                    psum += p0 + p1;
+                    const float p0 = exp2_approx(fmaf(sv[2 * e], a.scale_log2, -mr));
+                    const float p1 = exp2_approx(fmaf(sv[2 * e + 1], a.scale_log2, -mr));
                     pk[e] = pack_bf16(p0, p1);
+                    // the row sum adds the bf16 values PV multiplies, so the
+                    // output is an exactly normalised average of the values
+                    psum += bf16_lo(pk[e]) + bf16_hi(pk[e]);
                 }
                 tmem_st16u(tmem + lane_off + kSCol + (j & 1) * kBlockN + q * (SW / 2), pk);
                 tmem_wait_st();
@@ -768,6 +773,8 @@ extern "C" int medusa_tree_attention(const void* q, const void* k_cache, const v
         return fail(MEDUSA_ERR_INVALID_ARG, "tree_attention: null pointer");
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return fail(MEDUSA_ERR_INVALID_ARG, "tree_attention: q, caches and out must be 16-byte aligned");
+    if (!(scale > 0.f) || scale > 3.0e38f)
+        return fail(MEDUSA_ERR_INVALID_ARG, "tree_attention: scale must be positive and finite");
     const int W = (N + 63) / 64;
     cudaStream_t st = as_stream(stream);
     if (dtype == MEDUSA_F32) {

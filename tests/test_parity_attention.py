@@ -54,6 +54,25 @@ def test_attention_full_compare(medusa, kind, B, Hq, Hkv, D, lens, Lmax, dtype):
     assert np.abs(got - ref).max() <= TOL
 
 
+@pytest.mark.parametrize("kind,B,Hq,Hkv,D,lens,Lmax", [
+    # many (sequence, KV head, query block) units: odd block count (341 rows),
+    # even count (512 rows x GQA 2), D 64 and 128, empty and ragged prefixes
+    # (an empty prefix leaves a row a handful of keys, where the bf16 rounding
+    # of the probabilities matters most)
+    ("dense", 2, 38, 38, 128, [100, 300], 700),
+    ("dense", 2, 38, 38, 64, [0, 250], 600),
+    ("max512", 1, 76, 38, 64, [129], 650),
+])
+def test_attention_many_blocks(medusa, kind, B, Hq, Hkv, D, lens, Lmax):
+    t = _tree(kind)
+    x = W.attention_inputs(seed=7 + B + D, B=B, N=t["N"], Hq=Hq, Hkv=Hkv, D=D, Lmax=Lmax, dtype="bf16")
+    kv_len = np.array(lens, np.int32)
+    scale = float(np.float32(1 / np.sqrt(D)))
+    got = _run(medusa, x, kv_len, t, scale)
+    ref = O.tree_attention(x["q"], x["k_cache"], x["v_cache"], kv_len, t["mask"], "bf16", scale)
+    assert np.abs(got - ref).max() <= TOL
+
+
 def _sample_rows(B, N, Hq, n, seed):
     rng = np.random.default_rng(seed)
     rows = np.stack([rng.integers(0, B, n), rng.integers(0, N, n), rng.integers(0, Hq, n)], 1)
