@@ -466,12 +466,16 @@ int oracle_verify_tree(const float* logits, const int32_t* cand, const int32_t* 
 /* is the n-th output of the generator started from state s.                  */
 /*   f(x)    = sm_next(x, 1)                                                  */
 /*   row key = f(f(f(f(f(seed) ^ stream) ^ b) ^ round) ^ pos)                 */
-/*   h_v     = sm_next(row key, v + 1)                                        */
-/*   U(h)    = (h >> 40) / 2^24 in [0,1);   Up(h) = ((h >> 40) + 1) / 2^24     */
+/*   U(h)    = (h >> 40) / 2^24 in [0,1)  (accept uniforms: h = sm_next(row   */
+/*             key, 1))                                                       */
+/*   race uniforms: one output serves two vocab entries, h_m = sm_next(row    */
+/*             key, m + 1) for entries 2m and 2m + 1; entry 2m takes bits     */
+/*             40..63 and entry 2m + 1 bits 16..39:                           */
+/*             Up_v = (bits_v + 1) / 2^24 in (0, 1]                           */
 /* streams: 1 = accept uniform (v = 0), 2 = residual draw, 3 = bonus draw;   */
 /* pos counts draft positions from 1.                                         */
 /* Accept test: u * q_i(x_i) < p_i(x_i), exact in double (u has 24 bits).     */
-/* Draw from weights w: argmin over w_v > 0 of -ln(Up(h_v)) / w_v, lowest v   */
+/* Draw from weights w: argmin over w_v > 0 of -ln(Up_v) / w_v, lowest v      */
 /* on ties (the exponential race); if no weight is positive, argmax of p_i.   */
 /* ------------------------------------------------------------------------- */
 #define SM_GAMMA 0x9E3779B97F4A7C15ULL
@@ -493,7 +497,12 @@ uint64_t oracle_row_key(uint64_t seed, uint64_t stream, uint64_t b, uint64_t rou
 }
 
 static double unif(uint64_t h) { return (double)(h >> 40) * (1.0 / 16777216.0); }
-static double unif_pos(uint64_t h) { return (double)((h >> 40) + 1) * (1.0 / 16777216.0); }
+/* Up_v of the race: two disjoint 24-bit fields of one generator output */
+static double race_unif(uint64_t key, int v) {
+    const uint64_t h = sm_next(key, (uint64_t)(v >> 1) + 1);
+    const uint64_t bits = (v & 1) ? ((h >> 16) & 0xFFFFFFULL) : (h >> 40);
+    return (double)(bits + 1) * (1.0 / 16777216.0);
+}
 
 /* exponential race over weights w[V]; returns the chosen token, and the gap
  * between the best and second-best keys relative to the best (for tie checks) */
@@ -502,7 +511,7 @@ static int race(const double* w, const float* p_fallback, int V, uint64_t key, d
     double k1 = INFINITY, k2 = INFINITY;
     for (int v = 0; v < V; ++v) {
         if (!(w[v] > 0.0)) continue;
-        double kv = -log(unif_pos(sm_next(key, (uint64_t)v + 1))) / w[v];
+        double kv = -log(race_unif(key, v)) / w[v];
         if (kv < k1) { k2 = k1; k1 = kv; best = v; }
         else if (kv < k2) k2 = kv;
     }
