@@ -216,8 +216,17 @@ __device__ __forceinline__ uint64_t row_key(uint64_t seed, uint64_t stream, uint
     return sm64(x ^ pos, 1);
 }
 __device__ __forceinline__ float u24(uint64_t h) { return (float)(h >> 40) * (1.0f / 16777216.0f); }
-__device__ __forceinline__ float u24p(uint64_t h) {
-    return (float)((h >> 40) + 1) * (1.0f / 16777216.0f);
+// The race's uniforms: one generator output h_m = next(key, m + 1) serves the
+// vocab entries 2m (bits 40..63) and 2m + 1 (bits 16..39); U+ = (bits + 1) / 2^24.
+__device__ __forceinline__ float race_u_even(uint64_t h) {
+    return (float)((uint32_t)(h >> 40) + 1u) * (1.0f / 16777216.0f);
+}
+__device__ __forceinline__ float race_u_odd(uint64_t h) {
+    return (float)(((uint32_t)(h >> 16) & 0xFFFFFFu) + 1u) * (1.0f / 16777216.0f);
+}
+__device__ __forceinline__ float race_u(uint64_t key, int v) {
+    const uint64_t h = sm_mix(key + (uint64_t)((v >> 1) + 1) * kSmGamma);
+    return (v & 1) ? race_u_odd(h) : race_u_even(h);
 }
 
 constexpr int kChainThreads = 256;
@@ -271,17 +280,42 @@ __global__ void __launch_bounds__(kChainThreads) chain_scan_kernel(
     // w the weight) and compared by cross-multiplication (one division per
     // thread, not per element).  The largest p is tracked without its index:
     // the index is looked up afterwards, only when no weight is positive.
+    //
+    // Pruning: once the CTA has seen keys, kb bounds its best key from above.
+    // Since -ln U >= 1 - U, an element with (1 - U) > kb * w * (1 + 2^-10) has a
+    // key more than 2^-11 (relative) above a key already seen: it can neither
+    // win nor tie, so its logarithm and comparison are skipped (by the whole
+    // warp when no lane needs them).  The margin is far above the float32
+    // rounding of logf, the products and kb itself.
     float be = INFINITY, bw = 1.f, pm = -INFINITY;
     int bt = INT_MAX;
-    auto take = [&](float pv, float qv, int v, uint64_t z) {  // z = key + (v + 1) * gamma
+    float kb = INFINITY;
+    constexpr float kPruneMargin = 1.f + 1.f / 1024.f;
+    auto take = [&](float pv, float qv, int v, float u) {
         pm = fmaxf(pm, pv);
         const float w = bonus ? pv : pv - qv;
-        if (w > 0.f) {
-            const float e = -logf(u24p(sm_mix(z)));
-            const float lhs = e * bw, rhs = be * w;
-            if (lhs < rhs || (lhs == rhs && v < bt)) { be = e; bw = w; bt = v; }
+        const bool need = w > 0.f && !(1.f - u > kb * w * kPruneMargin);
+        if (__any_sync(__activemask(), need)) {
+            if (need) {
+                const float e = -logf(u);
+                const float lhs = e * bw, rhs = be * w;
+                if (lhs < rhs || (lhs == rhs && v < bt)) { be = e; bw = w; bt = v; }
+            }
         }
     };
+    __shared__ unsigned s_kb;
+    // the CTA's best key so far (keys are >= 0: their bit patterns order as
+    // unsigned integers); called by every thread
+    auto refresh_bound = [&]() {
+        float k = bt == INT_MAX ? INFINITY : be / bw;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) k = fminf(k, __shfl_xor_sync(0xffffffffu, k, o));
+        if ((threadIdx.x & 31) == 0) atomicMin(&s_kb, __float_as_uint(k));
+        __syncthreads();
+        kb = __uint_as_float(s_kb);
+    };
+    if (threadIdx.x == 0) s_kb = __float_as_uint(INFINITY);
+    __syncthreads();
     const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0 &&
                      (bonus || (reinterpret_cast<uintptr_t>(q) & 15u) == 0);
     if (vec) {
@@ -294,21 +328,31 @@ __global__ void __launch_bounds__(kChainThreads) chain_scan_kernel(
             pw[k] = v < v1 ? ld_stream16(pr + v) : make_uint4(0, 0, 0, 0);
             qw[k] = (v < v1 && !bonus) ? ld_stream16(qr + v) : make_uint4(0, 0, 0, 0);
         }
-        const uint64_t zstep = (uint64_t)(4 * kChainThreads) * kSmGamma;
-        uint64_t z = key + (uint64_t)(v0 + 4 * threadIdx.x + 1) * kSmGamma;
+        // entries v..v+3 (v a multiple of 4) use the outputs m = v/2 + 1 and
+        // v/2 + 2; the generator state is advanced by additions
+        const uint64_t zstep = (uint64_t)(2 * kChainThreads) * kSmGamma;
+        uint64_t z = key + (uint64_t)((v0 >> 1) + 2 * threadIdx.x + 1) * kSmGamma;
 #pragma unroll
         for (int k = 0; k < kPer; ++k, z += zstep) {
             const int v = v0 + 4 * (threadIdx.x + kChainThreads * k);
-            if (v < v1) {
-                take(__uint_as_float(pw[k].x), __uint_as_float(qw[k].x), v, z);
-                take(__uint_as_float(pw[k].y), __uint_as_float(qw[k].y), v + 1, z + kSmGamma);
-                take(__uint_as_float(pw[k].z), __uint_as_float(qw[k].z), v + 2, z + 2 * kSmGamma);
-                take(__uint_as_float(pw[k].w), __uint_as_float(qw[k].w), v + 3, z + 3 * kSmGamma);
+            const bool in = v < v1;
+            uint64_t h0 = 0;
+            if (in) {
+                h0 = sm_mix(z);
+                take(__uint_as_float(pw[k].x), __uint_as_float(qw[k].x), v, race_u_even(h0));
             }
+            if (k == 0) refresh_bound();  // after one element per thread
+            if (in) {
+                take(__uint_as_float(pw[k].y), __uint_as_float(qw[k].y), v + 1, race_u_odd(h0));
+                const uint64_t h1 = sm_mix(z + kSmGamma);
+                take(__uint_as_float(pw[k].z), __uint_as_float(qw[k].z), v + 2, race_u_even(h1));
+                take(__uint_as_float(pw[k].w), __uint_as_float(qw[k].w), v + 3, race_u_odd(h1));
+            }
+            if (k == 0) refresh_bound();  // after the first group of four
         }
     } else {
         for (int v = v0 + threadIdx.x; v < v1; v += kChainThreads)
-            take(pr[v], bonus ? 0.f : qr[v], v, key + (uint64_t)(v + 1) * kSmGamma);
+            take(pr[v], bonus ? 0.f : qr[v], v, race_u(key, v));
     }
     float bk = bt == INT_MAX ? INFINITY : be / bw;
 #pragma unroll
@@ -431,7 +475,7 @@ __global__ void __launch_bounds__(kRaceThreads) tree_race_kernel(
         for (int v = v0 + threadIdx.x; v < v1; v += kRaceThreads) {
             const float w = expf(row[v] * inv_t - m);
             if (w > 0.f) {
-                const float e = -logf(u24p(sm_mix(key + (uint64_t)(v + 1) * kSmGamma)));
+                const float e = -logf(race_u(key, v));
                 const float lhs = e * bw, rhs = be * w;
                 if (lhs < rhs || (lhs == rhs && v < bt)) { be = e; bw = w; bt = v; }
             }
