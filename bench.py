@@ -54,7 +54,7 @@ WORKLOAD = ("vicuna7b-shaped medusa step, batch 1: hidden 4096, vocab 32000, 5 h
 # DRAM bytes per launch of the heads call, from the ncu capture summarised in
 # profiles/ (dram__bytes_read.sum + dram__bytes_write.sum summed over its three
 # kernels), with the sha1 of heads.cu it was taken on; null once that file changes.
-HEADS_TRAFFIC = {"sha1": "981e10b213ab453486660c36df6f8300f3b3cf10", "bytes": 1479545387}
+HEADS_TRAFFIC = {"sha1": "08f4969426debbfde5bf581e1d7d48d425686e5b", "bytes": 1479522091}
 
 
 def _sha1(path):
@@ -247,32 +247,59 @@ class Step:
         rec(5)
 
 
+def _pack(tensors, device, pinned=False):
+    """One buffer holding `tensors` at 256-byte aligned offsets; returns the
+    buffer and views of it shaped like the inputs (contents copied in)."""
+    import torch
+    offs, off = [], 0
+    for t in tensors:
+        offs.append(off)
+        off = (off + t.numel() * t.element_size() + 255) // 256 * 256
+    buf = torch.empty(off, dtype=torch.uint8, device=device)
+    if pinned:
+        buf = buf.pin_memory()
+    views = []
+    for t, o in zip(tensors, offs):
+        v = buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views.append(v)
+    return buf, views
+
+
 def run_e2e(step, steps, warmup):
     """Same step through the C ABI with host buffers: per-step inputs copied from
-    pinned host memory, results read back, all inside the timed region."""
+    pinned host memory, results read back, all inside the timed region.  The
+    contiguous inputs (h, q, verifier logits, tree hidden states) travel as one
+    packed copy and the results as one packed read; the tree's K/V rows are
+    copied into their cache slots."""
     torch = step.torch
-    c = CFG
-    pin = lambda t: t.cpu().pin_memory()
     L = int(step.kv_len0[0].item())
     N = step.N
-    host = dict(h=pin(step.h), q=pin(step.q), vl=pin(step.vlogits), ht=pin(step.ht),
-                tk=pin(step.kc[:, :, L:L + N].contiguous()), tv=pin(step.vc[:, :, L:L + N].contiguous()))
-    outs = [step.acc["accept_len"], step.acc["best_node"], step.acc["path_nodes"],
-            step.acc["next_tok"], step.h_next]
-    host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    dev = step.h.device
+    # inputs: one device staging buffer the step reads from, and its pinned twin
+    names_in = ("h", "q", "vlogits", "ht")
+    dbuf_in, views = _pack([getattr(step, n) for n in names_in], dev)
+    for n, v in zip(names_in, views):
+        setattr(step, n, v)
+    hbuf_in, _ = _pack([getattr(step, n).cpu() for n in names_in], "cpu", pinned=True)
+    tk = step.kc[:, :, L:L + N].contiguous().cpu().pin_memory()
+    tv = step.vc[:, :, L:L + N].contiguous().cpu().pin_memory()
+    # results: the step writes them into one device buffer, read back in one copy
+    names_out = ("accept_len", "best_node", "path_nodes", "next_tok")
+    dbuf_out, outs = _pack([step.acc[n] for n in names_out] + [step.h_next], dev)
+    for n, v in zip(names_out, outs[:4]):
+        step.acc[n] = v
+    step.h_next = outs[4]
+    hbuf_out = torch.empty(dbuf_out.numel(), dtype=torch.uint8).pin_memory()
+    h2d = hbuf_in.numel() + tk.numel() * tk.element_size() + tv.numel() * tv.element_size()
+    d2h = hbuf_out.numel()
 
     def one():
-        step.h.copy_(host["h"], non_blocking=True)
-        step.q.copy_(host["q"], non_blocking=True)
-        step.vlogits.copy_(host["vl"], non_blocking=True)
-        step.ht.copy_(host["ht"], non_blocking=True)
-        step.kc[:, :, L:L + N].copy_(host["tk"], non_blocking=True)
-        step.vc[:, :, L:L + N].copy_(host["tv"], non_blocking=True)
+        dbuf_in.copy_(hbuf_in, non_blocking=True)
+        step.kc[:, :, L:L + N].copy_(tk, non_blocking=True)
+        step.vc[:, :, L:L + N].copy_(tv, non_blocking=True)
         step.run()
-        for o, ho in zip(outs, host_out):
-            ho.copy_(o, non_blocking=True)
+        hbuf_out.copy_(dbuf_out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     for _ in range(warmup):
