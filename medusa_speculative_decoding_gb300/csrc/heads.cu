@@ -548,8 +548,8 @@ extern "C" int medusa_heads_topk_static(const void* h, const void* w1, const voi
     if (rc) return rc;
     // No scratch byte needs to start at zero: the call writes every byte whose
     // value it uses (z before the vocab pass, the slice lists before the merge;
-    // the padding rows of the z planes at batches above 8 are loaded but feed
-    // only accumulator columns that are never read).
+    // on the tensor-core path the padding rows of the z planes are loaded but
+    // feed only accumulator columns that are never read).
     return medusa_heads_topk(h, w1, b1, w2, dtype, B, K, H, V, topk, topk_idx, topk_val, logits, ws,
                              (size_t)MEDUSA_HEADS_STATIC_SCRATCH_BYTES, stream);
 }

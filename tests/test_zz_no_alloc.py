@@ -57,7 +57,9 @@ def test_static_scratch_matches_workspace_entry(medusa, cases):
 
 
 def test_static_scratch_rejects_shapes_beyond_its_maximum(medusa):
-    # B=8, K=64, H=4096 needs 8 MiB of float32 z alone: refused, nothing launched
+    # B=8, K=64, H=4096 needs far more than the 4 MiB maximum (25 MB of z planes
+    # on the tensor cores, 8 MiB of float32 z on CUDA cores): refused, nothing
+    # launched
     L = medusa.lib()
     rc = L.medusa_heads_topk_static(None, None, None, None, 1, 8, 64, 4096, 32000, 8, None, None,
                                     None, None)
