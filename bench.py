@@ -17,7 +17,8 @@ CUDA graph with tree attention over 32 layers' caches), "attention_workloads" (t
 alone at the batch-8 ragged and batch-4 KV-8192 shapes), "chain_acceptance"
 (speculative-sampling acceptance at batch 64, vocab 128256), "heads_batches"
 (a batch sweep of the heads alone: batch 1-64 at hidden 4096, batch 8 at
-hidden 5120) and
+hidden 5120), "tree_sizes" (the step with the sparse 64-node and the dense
+341-node tree at equal planted acceptance) and
 "verify_projection": the fused
 verification projection (lm_head x tree hidden states on the tensor cores,
 reduced to acceptance without writing logits) timed at the step's shapes and at
@@ -218,6 +219,45 @@ class Step:
         self.vlogits = td(W.planted_logits(2, cand, t["parent"], V, c["alpha"]))
         # heads 2 (W1, W2 with the merge) + tree 1 + attention 1-2 + verify 2 + compaction 1
         self.launches = 2 + 1 + (2 if self.ws_att_n > 0 else 1) + 2 + 1
+
+    def with_tree(self, t, seed=3):
+        """A copy of this step that verifies tree `t` instead (same weights, batch,
+        KV length and planted acceptance): tree tables, queries, caches with
+        room for the tree, tree hidden states and verifier logits planted around
+        the new tree's candidates.  Set-up only; nothing here is timed."""
+        import copy
+        torch, M, c = self.torch, self.M, CFG
+        s = copy.copy(self)
+        dev = self.h.device
+        B, V = c["B"], c["V"]
+        s.t = t
+        s.N, s.Dmax = t["N"], t["max_depth"]
+        s.depth, s.rank, s.parent = self.td(t["depth"]), self.td(t["rank"]), self.td(t["parent"])
+        s.mask = self.td(t["mask"])
+        Lmax = int(self.kv_len0.max().item()) + s.N
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        s.q = torch.randn((B, s.N, c["Hq"], c["D"]), device=dev, generator=g).to(self.q.dtype)
+        s.kc = torch.randn((B, c["Hkv"], Lmax, c["D"]), device=dev, generator=g).to(self.kc.dtype)
+        s.vc = torch.randn((B, c["Hkv"], Lmax, c["D"]), device=dev, generator=g).to(self.vc.dtype)
+        s.ht = torch.randn((B, s.N, c["H"]), device=dev, generator=g).to(self.ht.dtype)
+        s.kv_len = self.kv_len0.clone()
+        i32 = torch.int32
+        s.cand = torch.empty((B, s.N), dtype=i32, device=dev)
+        s.att_out = torch.empty((B, s.N, c["Hq"], c["D"]), dtype=torch.float32, device=dev)
+        s.acc = dict(accept_len=torch.empty(B, dtype=i32, device=dev), best_node=torch.empty(B, dtype=i32, device=dev),
+                     path_nodes=torch.empty((B, s.Dmax + 1), dtype=i32, device=dev),
+                     next_tok=torch.empty(B, dtype=i32, device=dev))
+        s.h_next = torch.empty_like(self.h_next)
+        s.src = torch.empty((B, s.Dmax + 1), dtype=i32, device=dev)
+        s.ws_att_n = M.tree_attention_workspace(B, s.N, c["Hq"], c["Hkv"], c["D"], Lmax)
+        s.ws_att = torch.empty(max(16, s.ws_att_n), dtype=torch.uint8, device=dev)
+        s.ws_ver = torch.empty(max(16, M.verify_accept_workspace(B, s.N, V)), dtype=torch.uint8, device=dev)
+        s.heads()
+        M.build_tree(s.idx, s.root, s.depth, s.rank, out=s.cand)
+        s.vlogits = self.td(W.planted_logits(2, s.cand.cpu().numpy(), t["parent"], V, c["alpha"]))
+        s.launches = 2 + 1 + (2 if s.ws_att_n > 0 else 1) + 2 + 1
+        return s
 
     def heads(self):
         c = CFG
@@ -511,6 +551,40 @@ def measure_step_graph(step, layers=32, iters=200, warmup=5):
                                     "gbs": abytes / (us_att * 1e-6) / 1e9,
                                     "frac_hbm": abytes / (us_att * 1e-6) / 1e9 / hbm,
                                     "method": f"graph of {layers} back-to-back calls, one cache per layer"}}
+
+
+def measure_tree_sizes(step, iters=200, warmup=10):
+    """The step verifying the sparse 64-node tree and, at the same batch, KV
+    length and planted acceptance, the dense 341-node tree (top-4 of heads 1-4,
+    Cartesian product), each timed over `iters` back-to-back steps with events at
+    the two ends.  Acceptance is planted along the rank-0 chain in both (alpha
+    0.8), so both accept the same expected number of tokens: the comparison is
+    the cost side of choosing the smaller tree."""
+    import torch
+    M = step.M
+    dense_paths = np.array([[a, b, x, y] for a in range(4) for b in range(4) for x in range(4)
+                            for y in range(4)], np.int32)
+    out = {}
+    for name, make in (("sparse64", lambda: step), ("dense341", lambda: step.with_tree(M.tree_layout(dense_paths, 4)))):
+        s = make()
+        for _ in range(warmup):
+            s.run()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            s.run()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / iters
+        # expected tokens per step of the planted acceptance: sum of alpha^i up to
+        # the tree's depth (the same 3.36 for both depth-4 trees)
+        tokens = sum(CFG["alpha"] ** i for i in range(s.Dmax + 1))
+        out[name] = {"nodes": s.N, "us_per_step": us, "steps_per_s": 1e6 / us,
+                     "tree_tokens_verified_per_s": s.N * 1e6 / us, "expected_tokens_per_step": tokens,
+                     "expected_tokens_per_s": tokens * 1e6 / us}
+        del s
+    return out
 
 
 def measure_heads_batches(dev, iters=10, warmup=2):
@@ -815,6 +889,7 @@ def main():
     e2e_val = world * max(20, K // 4) / e2e_s
 
     graph = measure_step_graph(step) if world == 1 or rank == 0 else None
+    trees = measure_tree_sizes(step) if world == 1 or rank == 0 else None
     proj = measure_projection(dev) if world == 1 or rank == 0 else None
     att_w = measure_attention_workloads(dev) if world == 1 or rank == 0 else None
     chain = measure_chain(dev) if world == 1 or rank == 0 else None
@@ -843,6 +918,7 @@ def main():
             "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
             "step_ms_distribution": step_dist,
             "step_graph_32_layers": graph,
+            "tree_sizes": trees,
             "verify_projection": proj,
             "attention_workloads": att_w,
             "chain_acceptance": chain,
