@@ -579,7 +579,8 @@ def measure_tree_sizes(step, iters=200, warmup=10):
         us = a.elapsed_time(b) * 1e3 / iters
         # expected tokens per step of the planted acceptance: sum of alpha^i up to
         # the tree's depth (the same 3.36 for both depth-4 trees)
-        tokens = sum(CFG["alpha"] ** i for i in range(s.Dmax + 1))
+        depth = int(np.max(s.t["depth"]))  # the deepest node (the layout's cap may be larger)
+        tokens = sum(CFG["alpha"] ** i for i in range(depth + 1))
         out[name] = {"nodes": s.N, "us_per_step": us, "steps_per_s": 1e6 / us,
                      "tree_tokens_verified_per_s": s.N * 1e6 / us, "expected_tokens_per_step": tokens,
                      "expected_tokens_per_s": tokens * 1e6 / us}
