@@ -46,7 +46,7 @@ sys.path.insert(0, ROOT)
 
 import workloads as W  # noqa: E402
 
-CFG = W.CONFIGS[2]
+CFG = W.WORKLOADS["h4096_b1_sparse64"]
 METRIC = "Medusa decode steps/s (tree tokens verified/s = steps/s x 64 nodes)"
 WORKLOAD = ("vicuna7b-shaped medusa step, batch 1: hidden 4096, vocab 32000, 5 heads, top-8, "
             "sparse 64-node tree, 32x128 attention over KV 2048 (one layer), greedy acceptance, "
@@ -86,7 +86,8 @@ def _tree_tables():
     return M.tree_layout(paths, 5)
 
 
-def make_inputs(seed=2):
+def make_inputs(seed=None):
+    seed = CFG["seed"] if seed is None else seed
     c = CFG
     t = _tree_tables()
     N = t["N"]
@@ -216,7 +217,7 @@ class Step:
         self.heads()
         self.M.build_tree(self.idx, self.root, self.depth, self.rank, out=self.cand)
         cand = self.cand.cpu().numpy()
-        self.vlogits = td(W.planted_logits(2, cand, t["parent"], V, c["alpha"]))
+        self.vlogits = td(W.planted_logits(CFG["seed"], cand, t["parent"], V, c["alpha"]))
         # heads 2 (W1, W2 with the merge) + tree 1 + attention 1-2 + verify 2 + compaction 1
         self.launches = 2 + 1 + (2 if self.ws_att_n > 0 else 1) + 2 + 1
 
@@ -255,7 +256,7 @@ class Step:
         s.ws_ver = torch.empty(max(16, M.verify_accept_workspace(B, s.N, V)), dtype=torch.uint8, device=dev)
         s.heads()
         M.build_tree(s.idx, s.root, s.depth, s.rank, out=s.cand)
-        s.vlogits = self.td(W.planted_logits(2, s.cand.cpu().numpy(), t["parent"], V, c["alpha"]))
+        s.vlogits = self.td(W.planted_logits(CFG["seed"], s.cand.cpu().numpy(), t["parent"], V, c["alpha"]))
         s.launches = 2 + 1 + (2 if s.ws_att_n > 0 else 1) + 2 + 1
         return s
 
@@ -698,7 +699,7 @@ class OracleSample:
                              1).astype(np.int32)
         self.cand = O.build_tree(W.random_topk_lists(2, c["B"], c["K"], c["topk"], c["V"]), inp["root"],
                                  t["depth"], t["rank"])
-        self.vlogits = W.planted_logits(2, self.cand, t["parent"], c["V"], c["alpha"])
+        self.vlogits = W.planted_logits(CFG["seed"], self.cand, t["parent"], c["V"], c["alpha"])
         self.hd = inp["heads"]
 
     def step(self, k):
@@ -937,8 +938,9 @@ def main():
     return 0
 
 
-def make_inputs_host_only(seed=2):
+def make_inputs_host_only(seed=None):
     """Inputs of the reference arm: the same generator, tree from the oracle."""
+    seed = CFG["seed"] if seed is None else seed
     from oracle import oracle as O
     c = CFG
     t = O.tree_layout(O.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5)

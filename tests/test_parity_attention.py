@@ -81,18 +81,20 @@ def _sample_rows(B, N, Hq, n, seed):
     return rows.astype(np.int32)
 
 
-@pytest.mark.parametrize("cfg,kind", [(2, "sparse64"), (3, "sparse64"), (4, "dense"), (4, "sparse64")])
-def test_attention_full_size_sampled(medusa, cfg, kind):
-    c = W.CONFIGS[cfg]
+@pytest.mark.parametrize("name,kind", [("h4096_b1_sparse64", "sparse64"), ("h5120_b8_ragged", "sparse64"),
+                                       ("h4096_b4_kv8192", "dense"), ("h4096_b4_kv8192", "sparse64")])
+def test_attention_full_size_sampled(medusa, name, kind):
+    c = W.WORKLOADS[name]
+    seed = c["seed"]
     t = _tree(kind)
     N = t["N"]
-    kv_len = W.kv_lengths(cfg, c["B"], c["L_lo"], c["L_hi"])
+    kv_len = W.kv_lengths(seed, c["B"], c["L_lo"], c["L_hi"])
     Lmax = c["L_hi"] + N
-    x = W.attention_inputs(seed=cfg, B=c["B"], N=N, Hq=c["Hq"], Hkv=c["Hkv"], D=c["D"], Lmax=Lmax,
+    x = W.attention_inputs(seed=seed, B=c["B"], N=N, Hq=c["Hq"], Hkv=c["Hkv"], D=c["D"], Lmax=Lmax,
                            dtype=c["dtype"])
     scale = float(np.float32(1 / np.sqrt(c["D"])))
     got = _run(medusa, x, kv_len, t, scale)
-    rows = _sample_rows(c["B"], N, c["Hq"], 96, seed=cfg)
+    rows = _sample_rows(c["B"], N, c["Hq"], 96, seed=seed)
     ref = O.tree_attention(x["q"], x["k_cache"], x["v_cache"], kv_len, t["mask"], c["dtype"], scale,
                            rows=rows)
     sel = got[rows[:, 0], rows[:, 1], rows[:, 2]]

@@ -49,7 +49,7 @@ def test_chain_small(medusa, B, gamma, V, sigma):
 
 @pytest.mark.parametrize("gamma,sigma", [(0, 0.1), (1, 0.5), (4, 1.0), (8, 0.1), (32, 0.5)])
 def test_chain_full_size(medusa, gamma, sigma):
-    c = W.CONFIGS[5]
+    c = W.WORKLOADS["chain_b64_v128256"]
     x = W.chain_inputs(seed=5, B=c["B"], gamma=gamma, V=c["V"], sigma=sigma)
     for rnd in range(2):
         n_acc, out = _gpu(medusa, x, 99, rnd)

@@ -70,10 +70,11 @@ def test_zero_init_heads_reproduce_lm_head(medusa):
         topk_near_tie_ok(idx[:, k], ridx, lm)
 
 
-@pytest.mark.parametrize("cfg,sample", [(2, None), (3, [0, 5]), (4, [2])])
-def test_heads_full_size(medusa, cfg, sample):
-    c = W.CONFIGS[cfg]
-    x = W.heads_inputs(seed=cfg, B=c["B"], H=c["H"], V=c["V"], K=c["K"], dtype=c["dtype"])
+@pytest.mark.parametrize("name,sample", [("h4096_b1_sparse64", None), ("h5120_b8_ragged", [0, 5]),
+                                         ("h4096_b4_kv8192", [2])])
+def test_heads_full_size(medusa, name, sample):
+    c = W.WORKLOADS[name]
+    x = W.heads_inputs(seed=c["seed"], B=c["B"], H=c["H"], V=c["V"], K=c["K"], dtype=c["dtype"])
     idx, val, lg = _run(medusa, x, c["topk"])
     rows = list(range(c["B"])) if sample is None else sample
     ref = O.heads_logits(x["h"][rows], x["w1"], x["b1"], x["w2"], c["dtype"])

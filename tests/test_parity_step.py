@@ -19,19 +19,20 @@ def _tree(c):
     return O.tree_layout(O.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5)
 
 
-@pytest.mark.parametrize("cfg", [1, 2])
-def test_full_step(medusa, cfg):
+@pytest.mark.parametrize("name", ["tiny_h256_v1000_f32", "h4096_b1_sparse64"])
+def test_full_step(medusa, name):
     M = medusa
-    c = W.CONFIGS[cfg]
+    c = W.WORKLOADS[name]
+    seed = c["seed"]
     t = _tree(c)
     N, Dmax = t["N"], t["max_depth"]
     dt = c["dtype"]
-    heads = W.heads_inputs(cfg, c["B"], c["H"], c["V"], c["K"], dt)
-    kv_len = W.kv_lengths(cfg, c["B"], c["L_lo"], c["L_hi"])
+    heads = W.heads_inputs(seed, c["B"], c["H"], c["V"], c["K"], dt)
+    kv_len = W.kv_lengths(seed, c["B"], c["L_lo"], c["L_hi"])
     Lmax = c["L_hi"] + N
-    att = W.attention_inputs(cfg, c["B"], N, c["Hq"], c["Hkv"], c["D"], Lmax, dt)
-    ht = W.hidden_tree(cfg, c["B"], N, c["H"], dt)
-    root = W.root_tokens(cfg, c["B"], c["V"])
+    att = W.attention_inputs(seed, c["B"], N, c["Hq"], c["Hkv"], c["D"], Lmax, dt)
+    ht = W.hidden_tree(seed, c["B"], N, c["H"], dt)
+    root = W.root_tokens(seed, c["B"], c["V"])
     scale = float(np.float32(1 / np.sqrt(c["D"])))
 
     # oracle step
@@ -39,7 +40,7 @@ def test_full_step(medusa, cfg):
     ref_idx, _ = O.topk(ref_logits, c["topk"])
     ref_cand = O.build_tree(ref_idx, root, t["depth"], t["rank"])
     ref_att = O.tree_attention(att["q"], att["k_cache"], att["v_cache"], kv_len, t["mask"], dt, scale)
-    vlogits = W.planted_logits(cfg, ref_cand, t["parent"], c["V"], c["alpha"])
+    vlogits = W.planted_logits(seed, ref_cand, t["parent"], c["V"], c["alpha"])
     ref_acc = O.verify_tree(vlogits, ref_cand, t["parent"], t["depth"], Dmax)
     ref_k, ref_v, ref_kl, ref_hn, ref_src = O.kv_compact(
         att["k_cache"], att["v_cache"], kv_len, ref_acc["path_nodes"], ref_acc["accept_len"],

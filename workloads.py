@@ -35,20 +35,21 @@ STREAMS = {
 }
 
 # name -> shape and dtype of the five workloads.
-CONFIGS = {
-    1: dict(name="tiny-fp32", dtype="f32", B=1, H=256, V=1000, K=3, topk=3,
+# The workloads, named by shape; each draws its inputs from its own seed.
+WORKLOADS = {
+    "tiny_h256_v1000_f32": dict(seed=1, dtype="f32", B=1, H=256, V=1000, K=3, topk=3,
             tree="product", tree_ranks=(2, 3), Hq=4, Hkv=4, D=64,
             L_lo=128, L_hi=128, accept="greedy", alpha=0.8, w_std=0.02),
-    2: dict(name="vicuna7b-b1", dtype="bf16", B=1, H=4096, V=32000, K=5, topk=8,
+    "h4096_b1_sparse64": dict(seed=2, dtype="bf16", B=1, H=4096, V=32000, K=5, topk=8,
             tree="sparse64", Hq=32, Hkv=32, D=128, L_lo=2048, L_hi=2048,
             accept="greedy", alpha=0.8, w_std=0.02),
-    3: dict(name="13b-b8-ragged", dtype="bf16", B=8, H=5120, V=32000, K=5, topk=8,
+    "h5120_b8_ragged": dict(seed=3, dtype="bf16", B=8, H=5120, V=32000, K=5, topk=8,
             tree="sparse64", Hq=40, Hkv=40, D=128, L_lo=1024, L_hi=4096,
             accept="greedy", alpha=0.8, w_std=0.02),
-    4: dict(name="dense-vs-sparse-b4", dtype="bf16", B=4, H=4096, V=32000, K=5,
+    "h4096_b4_kv8192": dict(seed=4, dtype="bf16", B=4, H=4096, V=32000, K=5,
             topk=8, tree="dense", tree_ranks=(4, 4, 4, 4), Hq=32, Hkv=32, D=128,
             L_lo=8192, L_hi=8192, accept="typical", logit_std=3.0, w_std=0.02),
-    5: dict(name="chain-b64", dtype="f32", B=64, V=128256, sigmas=(0.1, 0.5, 1.0),
+    "chain_b64_v128256": dict(seed=5, dtype="f32", B=64, V=128256, sigmas=(0.1, 0.5, 1.0),
             gamma_max=32, ql_std=2.0),
 }
 
