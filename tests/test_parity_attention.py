@@ -22,6 +22,8 @@ def _tree(kind):
         return O.tree_layout(O.product_tree_paths((4, 4, 4, 4)), 4)
     if kind == "small":
         return O.tree_layout(O.sparse_tree_paths(20, 4, 4, 0.6, 0.5), 4)
+    if kind == "root":  # the root alone: plain decode attention over the prefix and itself
+        return O.tree_layout(O.sparse_tree_paths(1, 4, 4, 0.6, 0.5), 4)
     if kind == "max512":  # the largest tree the entry point takes: 512 nodes, 8 mask words
         return O.tree_layout(O.sparse_tree_paths(512, 8, 8, 0.6, 0.5), 8)
     raise KeyError(kind)
@@ -42,6 +44,8 @@ def _run(M, x, kv_len, t, scale):
     ("dense", 1, 2, 2, 128, [300], 700, "bf16"),
     ("c1", 4, 4, 4, 64, [1, 63, 64, 65], 80, "bf16"),
     ("max512", 2, 2, 2, 128, [0, 200], 720, "bf16"),
+    ("root", 2, 4, 4, 128, [0, 100], 110, "bf16"),
+    ("root", 1, 8, 2, 64, [300], 310, "bf16"),
     ("max512", 1, 4, 2, 64, [129], 650, "f32"),
 ])
 def test_attention_full_compare(medusa, kind, B, Hq, Hkv, D, lens, Lmax, dtype):

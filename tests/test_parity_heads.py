@@ -28,6 +28,7 @@ def _run(M, x, topk):
     (5, 264, 777, 4, 5, "f32", 1e-5),
     (2, 16384, 300, 1, 4, "bf16", 2e-2),    # largest hidden size (B * H = 32768)
     (1, 128, 300, 64, 4, "bf16", 2e-2),     # largest head count
+    (1, 8, 16, 1, 16, "f32", 1e-5),         # smallest hidden size, top-k of the whole vocab
     # bf16 batches 3-64 with H % 128 == 0 run on the tensor cores, the batch
     # padded to a multiple of 16 (planes at columns [0, Bp), [Bp, 2Bp),
     # [2Bp, 3Bp)): ragged vocab tiles, heads split across CTAs, runs that cross
@@ -46,6 +47,7 @@ def _run(M, x, topk):
     (64, 256, 1000, 5, 8, "bf16", 2e-2),
     (3, 16384, 300, 1, 4, "bf16", 2e-2),    # largest hidden size on the tensor cores
     (4, 128, 300, 64, 4, "bf16", 2e-2),     # largest head count on the tensor cores
+    (3, 128, 16, 2, 16, "bf16", 2e-2),      # vocab below one 128-row tile, top-k of all of it
 ])
 def test_heads_small(medusa, B, H, V, K, topk, dtype, tol):
     x = W.heads_inputs(seed=B * 7 + K, B=B, H=H, V=V, K=K, dtype=dtype, b1_std=0.5)

@@ -19,6 +19,8 @@ def _tree(kind):
         return O.tree_layout(O.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5)
     if kind == "dense":
         return O.tree_layout(O.product_tree_paths((4, 4, 4, 4)), 4)
+    if kind == "root":  # no candidates: the step yields the root's next token only
+        return O.tree_layout(O.sparse_tree_paths(1, 4, 4, 0.6, 0.5), 4)
     raise KeyError(kind)
 
 
@@ -38,7 +40,8 @@ KEYS = ("accept_len", "best_node", "path_nodes", "next_tok")
 
 
 @pytest.mark.parametrize("kind,B,V,K,k", [("c1", 1, 1000, 3, 3), ("sparse64", 1, 32000, 5, 8),
-                                          ("sparse64", 8, 32000, 5, 8), ("dense", 2, 5003, 4, 4)])
+                                          ("sparse64", 8, 32000, 5, 8), ("dense", 2, 5003, 4, 4),
+                                          ("root", 3, 1000, 3, 3)])
 def test_greedy_planted_exact(medusa, kind, B, V, K, k):
     t = _tree(kind)
     for seed in range(3):
