@@ -20,9 +20,9 @@
 // with probability min(1, p(x)/q(x)); at the first rejection draw from
 // max(0, p - q) normalised; if all are accepted draw a bonus token from the
 // next p.
-//   chain_scan_kernel   : finds the first rejection of its sequence, then runs
-//                         the exponential race over one vocab chunk of the row
-//                         to draw from
+//   chain_first_kernel  : one warp per sequence: the first rejection and the
+//                         key of the row to draw from
+//   chain_scan_kernel   : the exponential race over one vocab chunk of that row
 //   chain_finish_kernel : merges the chunk winners and writes the k + 1 tokens
 #include <float.h>
 #include <limits.h>
@@ -239,13 +239,19 @@ struct ChainPart {  // per (sequence, chunk)
     int pidx;
 };
 
-// First rejected position (1-based) of sequence b, or gamma + 1 if none.
-__device__ int first_reject(const float* p, const float* q, const int32_t* draft, int gamma, int V,
-                            int b, uint64_t seed, uint64_t round) {
-    __shared__ int s_first;
-    if (threadIdx.x == 0) s_first = gamma + 1;
-    __syncthreads();
-    for (int i = threadIdx.x; i < gamma; i += blockDim.x) {
+// One warp per sequence: the first rejected position (1-based; gamma + 1 if
+// every draft is accepted) and the key of the row the draw reads.  Done once
+// here so the scan CTAs can start their row loads right after the wait.
+__global__ void __launch_bounds__(256) chain_first_kernel(const float* __restrict__ p, const float* __restrict__ q,
+                                                          const int32_t* __restrict__ draft, int B, int gamma, int V,
+                                                          uint64_t seed, uint64_t round, int* __restrict__ firsts,
+                                                          uint64_t* __restrict__ keys) {
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (b >= B) return;
+    int first = gamma + 1;
+    for (int i = lane; i < gamma; i += 32) {
         const int x = draft[(size_t)b * gamma + i];
         bool accept = false;
         if (x >= 0 && x < V) {
@@ -255,26 +261,29 @@ __device__ int first_reject(const float* p, const float* q, const int32_t* draft
             // sign of u*q - p with one rounding: equals the sign of the exact value
             accept = fmaf(u, qi, -pi) < 0.f;
         }
-        if (!accept) atomicMin(&s_first, i + 1);
+        if (!accept) first = min(first, i + 1);
     }
-    __syncthreads();
-    return s_first;
+    first = __reduce_min_sync(0xffffffffu, first);
+    if (lane == 0) {
+        const bool bonus = first > gamma;
+        firsts[b] = first;
+        keys[b] = row_key(seed, bonus ? 3 : 2, b, round, bonus ? gamma + 1 : first);
+    }
 }
 
 __global__ void __launch_bounds__(kChainThreads) chain_scan_kernel(
-    const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ draft,
-    int gamma, int V, int nchunk, uint64_t seed, uint64_t round, ChainPart* __restrict__ parts,
-    int* __restrict__ firsts) {
-    pdl_wait();
+    const float* __restrict__ p, const float* __restrict__ q,
+    int gamma, int V, int nchunk, ChainPart* __restrict__ parts, const int* __restrict__ firsts,
+    const uint64_t* __restrict__ keys) {
+    pdl_wait();  // the first rejections and draw keys come from chain_first_kernel
     pdl_trigger();
     const int c = blockIdx.x, b = blockIdx.y;
-    const int first = first_reject(p, q, draft, gamma, V, b, seed, round);
-    if (c == 0 && threadIdx.x == 0) firsts[b] = first;
+    const int first = firsts[b];
     const bool bonus = first > gamma;
     const int pos = bonus ? gamma + 1 : first;          // 1-based position drawn at
     const float* pr = p + ((size_t)b * (gamma + 1) + (pos - 1)) * V;
     const float* qr = bonus ? nullptr : q + ((size_t)b * gamma + (pos - 1)) * V;
-    const uint64_t key = row_key(seed, bonus ? 3 : 2, b, round, pos);
+    const uint64_t key = keys[b];
     const int v0 = c * kChainChunk, v1 = min(V, v0 + kChainChunk);
     // The thread's best race key is kept as the fraction be / bw (E = -ln U+,
     // w the weight) and compared by cross-multiplication (one division per
@@ -425,14 +434,15 @@ __global__ void __launch_bounds__(32) chain_finish_kernel(const ChainPart* __res
 
 struct ChainPlan {
     int nchunk;
-    size_t off_parts, off_first, ws_bytes;
+    size_t off_parts, off_first, off_keys, ws_bytes;
 };
 ChainPlan plan_chain(int B, int V) {
     ChainPlan p{};
     p.nchunk = (V + kChainChunk - 1) / kChainChunk;
     p.off_parts = 0;
     p.off_first = align_up((size_t)B * p.nchunk * sizeof(ChainPart), 256);
-    p.ws_bytes = align_up(p.off_first + (size_t)B * sizeof(int), 256);
+    p.off_keys = align_up(p.off_first + (size_t)B * sizeof(int), 256);
+    p.ws_bytes = align_up(p.off_keys + (size_t)B * sizeof(uint64_t), 256);
     return p;
 }
 
@@ -764,9 +774,13 @@ extern "C" int medusa_verify_accept_chain(const float* p, const float* q, const 
     if (!aligned16(ws)) return fail(MEDUSA_ERR_INVALID_ARG, "verify_accept_chain: ws must be 16-byte aligned");
     ChainPart* parts = reinterpret_cast<ChainPart*>(static_cast<char*>(ws) + plan.off_parts);
     int* firsts = reinterpret_cast<int*>(static_cast<char*>(ws) + plan.off_first);
+    uint64_t* keys = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + plan.off_keys);
     cudaStream_t st = as_stream(stream);
-    cudaError_t e = launch(chain_scan_kernel, dim3(plan.nchunk, B), dim3(kChainThreads), 0, st, p, q,
-                           draft, gamma, V, plan.nchunk, seed, round, parts, firsts);
+    cudaError_t e = launch(chain_first_kernel, dim3((B + 7) / 8), dim3(256), 0, st, p, q, draft, B, gamma, V,
+                           seed, round, firsts, keys);
+    if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "chain_first: launch failed: %s", cudaGetErrorString(e));
+    e = launch(chain_scan_kernel, dim3(plan.nchunk, B), dim3(kChainThreads), 0, st, p, q, gamma, V, plan.nchunk,
+               parts, (const int*)firsts, (const uint64_t*)keys);
     if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "chain_scan: launch failed: %s", cudaGetErrorString(e));
     e = launch(chain_finish_kernel, dim3(B), dim3(32), 0, st, (const ChainPart*)parts,
                (const int*)firsts, draft, gamma, plan.nchunk, n_acc, out_tok);
