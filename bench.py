@@ -191,6 +191,7 @@ class Step:
         self.root = td(inp["root"])
         self.depth, self.rank, self.parent = td(t["depth"]), td(t["rank"]), td(t["parent"])
         self.mask = td(t["mask"])
+        self.scale = 1.0 / float(np.sqrt(c["D"]))  # the softmax scale of the attention layer
         self.q = td(inp["att"]["q"])
         self.kc, self.vc = td(inp["att"]["k_cache"]), td(inp["att"]["v_cache"])
         self.kv_len0 = td(inp["kv_len"])
@@ -277,7 +278,8 @@ class Step:
         rec(1)
         M.build_tree(self.idx, self.root, self.depth, self.rank, out=self.cand)
         rec(2)
-        M.tree_attention(self.q, self.kc, self.vc, self.kv_len, self.mask, out=self.att_out, ws=self.ws_att)
+        M.tree_attention(self.q, self.kc, self.vc, self.kv_len, self.mask, self.scale, out=self.att_out,
+                         ws=self.ws_att)
         rec(3)
         M.verify_accept_tree(self.vlogits, self.cand, self.parent, self.depth, self.Dmax, out=self.acc,
                              ws=self.ws_ver)
@@ -462,7 +464,7 @@ def measure_attention_workloads(dev, iters=20, warmup=3):
         o = torch.empty(B, N, Hq, D, device=dev)
         ws = torch.empty(max(16, M.tree_attention_workspace(B, N, Hq, Hq, D, Lmax)), dtype=torch.uint8,
                          device=dev)
-        call = lambda: M.tree_attention(q, kc, vc, kl, mask, out=o, ws=ws)
+        call = lambda: M.tree_attention(q, kc, vc, kl, mask, 1.0 / np.sqrt(D), out=o, ws=ws)
         for _ in range(warmup):
             call()
         torch.cuda.synchronize()
@@ -511,7 +513,8 @@ def measure_step_graph(step, layers=32, iters=200, warmup=5):
         step.heads()
         M.build_tree(step.idx, step.root, step.depth, step.rank, out=step.cand)
         for l in range(layers):
-            M.tree_attention(step.q, kls[l], vls[l], step.kv_len, step.mask, out=step.att_out, ws=step.ws_att)
+            M.tree_attention(step.q, kls[l], vls[l], step.kv_len, step.mask, step.scale, out=step.att_out,
+                             ws=step.ws_att)
         M.verify_accept_tree(step.vlogits, step.cand, step.parent, step.depth, step.Dmax, out=step.acc,
                              ws=step.ws_ver)
         M.kv_compact(kc, vc, step.kv_len, step.acc["path_nodes"], step.acc["accept_len"], step.acc["best_node"],
@@ -542,7 +545,8 @@ def measure_step_graph(step, layers=32, iters=200, warmup=5):
     # every call reads its keys and values from HBM)
     def att():
         for l in range(layers):
-            M.tree_attention(step.q, kls[l], vls[l], step.kv_len, step.mask, out=step.att_out, ws=step.ws_att)
+            M.tree_attention(step.q, kls[l], vls[l], step.kv_len, step.mask, step.scale, out=step.att_out,
+                             ws=step.ws_att)
     step.kv_len.copy_(step.kv_len0)
     with torch.cuda.stream(s):
         att()

@@ -99,8 +99,12 @@ int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void*
  * process whose device memory is fully reserved by a pool it may not grow.
  *   - Every GPU that loads the library holds that array until process exit.
  *   - The first call on a device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress) and caches it; make that
- *     first call before any stream capture on the device.
+ *     array's device address (cudaGetSymbolAddress) and caches it with the
+ *     unique ID of the current CUDA context; make that first call before any
+ *     stream capture on the device.  A call in another context (after
+ *     cudaDeviceReset, or in a context the caller created) looks the address
+ *     up again, so that first call in the new context must also precede any
+ *     capture.
  *   - Shapes whose scratch exceeds the maximum (e.g. large B*K*H) return
  *     MEDUSA_ERR_UNSUPPORTED without launching anything.
  *   - All calls share the one array: calls whose GPU work overlaps (other
@@ -212,10 +216,11 @@ int medusa_verify_accept_tree(const float* logits, const int32_t* cand, const in
 /*                                                                           */
 /* accept_len, best_node and path_nodes as medusa_verify_accept_tree in      */
 /* MEDUSA_ACCEPT_TYPICAL mode.  next_tok is drawn from P = softmax(row / T)   */
-/* of the best node by the exponential race argmin_v -ln(U+(h_v)) / w_v,      */
-/* w_v = exp(row_v / T - max / T), lowest v on ties, with the SplitMix64      */
-/* keys of 4b: key = f(f(f(f(f(seed) ^ 4) ^ b) ^ round) ^ 0), h_v =           */
-/* next(key, v + 1).  Workspace from medusa_verify_sample_workspace.          */
+/* of the best node by the exponential race argmin_v -ln(U+_v) / w_v,         */
+/* w_v = exp(row_v / T - max / T), lowest v on ties, with the random numbers  */
+/* of 4b: key = f(f(f(f(f(seed) ^ 4) ^ b) ^ round) ^ 0) and U+_v taken from   */
+/* next(key, v/2 + 1) as 4b states.  Workspace from                           */
+/* medusa_verify_sample_workspace.                                            */
 /* ------------------------------------------------------------------------- */
 size_t medusa_verify_sample_workspace(int B, int N, int V);
 int medusa_verify_accept_tree_sample(const float* logits, const int32_t* cand, const int32_t* parent,
@@ -261,13 +266,17 @@ int medusa_verify_project_tree(const void* hidden_tree, const void* lm_head, med
 /* rejection a token is drawn from max(0, p_i - q_i) normalised and the round */
 /* ends; if all gamma are accepted a bonus token is drawn from p_{gamma+1}.   */
 /* Random numbers (SplitMix64, Steele-Lea-Flood 2014; next(s, n) = n-th      */
-/* output from state s):                                                      */
+/* output from state s, i.e. the mix of s + n * 0x9E3779B97F4A7C15):          */
 /*   f(x) = next(x, 1);  key = f(f(f(f(f(seed) ^ stream) ^ b) ^ round) ^ pos)  */
-/*   h_v = next(key, v + 1);  U = (h >> 40) / 2^24;  U+ = ((h >> 40) + 1)/2^24 */
-/*   u_i = U(h_0) with stream 1, pos i.  A draw from weights w is the         */
-/*   exponential race argmin_{w_v > 0} -ln(U+(h_v)) / w_v (lowest v on ties),  */
-/*   stream 2 pos i for the residual, stream 3 pos gamma+1 for the bonus;     */
-/*   with no positive weight it falls back to argmax p_i.                     */
+/*   accept uniform of draft i (from 1): u_i = (next(key, 1) >> 40) / 2^24    */
+/*     with stream 1, pos i.                                                  */
+/*   race uniforms: output h_m = next(key, m + 1) serves two vocab entries:   */
+/*     entry 2m uses bits 40..63 and entry 2m+1 uses bits 16..39 of h_m;      */
+/*     U+_v = (those 24 bits + 1) / 2^24, in (0, 1].                          */
+/*   A draw from weights w is the exponential race argmin_{w_v > 0}           */
+/*   -ln(U+_v) / w_v (lowest v on ties): stream 2 pos i for the residual at   */
+/*   rejected position i, stream 3 pos gamma+1 for the bonus; with no         */
+/*   positive weight it falls back to the lowest v holding the largest p.     */
 /*   p [B,gamma+1,V] float32; q [B,gamma,V] float32; draft [B,gamma] int32     */
 /*   n_acc [B] out; out_tok [B,gamma+1] out: accepted drafts, then the drawn  */
 /*   token, -1 padded (n_acc + 1 tokens).  gamma = 0 is allowed (q, draft may */

@@ -147,7 +147,9 @@ def tree_attention_workspace(B, N, Hq, Hkv, D, Lmax):
     return int(lib().medusa_tree_attention_workspace(B, N, Hq, Hkv, D, Lmax))
 
 
-def tree_attention(q, k_cache, v_cache, kv_len, mask, scale=None, out=None, ws=None, stream=None):
+def tree_attention(q, k_cache, v_cache, kv_len, mask, scale, out=None, ws=None, stream=None):
+    """Tree attention; `scale` multiplies q.k inside the softmax (the model's
+    choice, usually 1/sqrt(head dim)); it is passed to the library as given."""
     _need(q, "q")
     _need(k_cache, "k_cache", q.dtype)
     _need(v_cache, "v_cache", q.dtype)
@@ -155,8 +157,6 @@ def tree_attention(q, k_cache, v_cache, kv_len, mask, scale=None, out=None, ws=N
     _need(mask, "mask", torch.int64)
     B, N, Hq, D = q.shape
     Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
-    if scale is None:
-        scale = 1.0 / float(np.sqrt(D))
     o = out if out is not None else torch.empty((B, N, Hq, D), dtype=torch.float32, device=q.device)
     need = tree_attention_workspace(B, N, Hq, Hkv, D, Lmax)
     if ws is None:

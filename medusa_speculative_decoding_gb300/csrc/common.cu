@@ -78,6 +78,29 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+int current_context_id(unsigned long long* id) {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_current || !get_id) return fail(MEDUSA_ERR_CUDA, "the driver lacks cuCtxGetCurrent or cuCtxGetId");
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return fail(MEDUSA_ERR_CUDA, "cuCtxGetCurrent failed");
+    *id = 0;  // no context is current yet
+    if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return fail(MEDUSA_ERR_CUDA, "cuCtxGetId failed");
+    return MEDUSA_OK;
+}
+
 }  // namespace medusa
 
 extern "C" const char* medusa_last_error(void) { return medusa::g_msg; }

@@ -15,6 +15,9 @@ int fail(int code, const char* fmt, ...);
 int check_launch(const char* what);
 // Number of SMs of the current device (cached per device).
 int sm_count();
+// Unique ID (for the life of the process) of the calling thread's current CUDA
+// context, or 0 when no context is current yet.
+int current_context_id(unsigned long long* id);
 // Opt-in maximum dynamic shared memory per block of the current device.
 int max_smem_optin();
 

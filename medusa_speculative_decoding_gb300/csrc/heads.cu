@@ -499,8 +499,10 @@ extern "C" int medusa_heads_topk(const void* h, const void* w1, const void* b1, 
 // Every GPU that loads this library reserves that array until the process
 // exits.  Host code never passes the array's name to a kernel (in host code it
 // is only a stand-in symbol): the device address comes from
-// cudaGetSymbolAddress, looked up once per device on the first call made with
-// that device current.
+// cudaGetSymbolAddress with that device current.  The address is cached per
+// device together with the unique ID of the CUDA context it was looked up in;
+// a call made in another context (after cudaDeviceReset, or under a context the
+// caller created) looks it up again, so a stale address is never used.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_heads_static_scratch[MEDUSA_HEADS_STATIC_SCRATCH_BYTES];
 
@@ -508,6 +510,7 @@ namespace medusa {
 namespace {
 std::mutex g_static_mu;
 void* g_static_ptr[64];
+unsigned long long g_static_ctx[64];
 
 int static_scratch(void** out) {
     int dev = 0;
@@ -516,14 +519,21 @@ int static_scratch(void** out) {
         return fail(MEDUSA_ERR_CUDA, "heads_topk_static: cudaGetDevice failed: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 64)
         return fail(MEDUSA_ERR_UNSUPPORTED, "heads_topk_static: device index %d above 63", dev);
+    unsigned long long ctx = 0;
+    int rc = current_context_id(&ctx);
+    if (rc) return rc;
     std::lock_guard<std::mutex> lk(g_static_mu);
-    if (!g_static_ptr[dev]) {
+    if (!g_static_ptr[dev] || ctx == 0 || g_static_ctx[dev] != ctx) {
+        // the lookup also initialises the device's primary context when none
+        // is current yet
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_heads_static_scratch);
         if (e != cudaSuccess || !p)
             return fail(MEDUSA_ERR_CUDA, "heads_topk_static: cudaGetSymbolAddress failed: %s",
                         cudaGetErrorString(e));
+        if (ctx == 0 && (rc = current_context_id(&ctx)) != 0) return rc;
         g_static_ptr[dev] = p;
+        g_static_ctx[dev] = ctx;
     }
     *out = g_static_ptr[dev];
     return MEDUSA_OK;
