@@ -106,3 +106,73 @@ def test_lm_head_logits_closed_forms(dtype):
     got3 = O.lm_head_logits(conv(np.full((1, H), 0.5, np.float32)),
                             conv(np.repeat(t[:, None], H, 1)), dtype)
     np.testing.assert_array_equal(got3[0], H * 0.5 * t.astype(np.float64))
+
+
+def _perm_case(seed, B=3, K=3, H=12, V=17):
+    """Heads whose W1_k = s * P_k for permutation matrices P_k (row i holds a 1
+    at column pi_k(i), so (W1_k h)_i = s * h[pi_k(i)]) and whose W2_k rows are
+    one-hot: W2_k[v] = e_{rho_k(v)}.  No P_k is symmetric, and pi_k != rho_k."""
+    rng = np.random.default_rng(seed)
+    pis = [rng.permutation(H) for _ in range(K)]
+    for p in pis:
+        assert not np.array_equal(p[p], np.arange(H))  # P_k is not its own transpose
+    rhos = [rng.integers(0, H, V) for _ in range(K)]
+    h = (rng.integers(-24, 25, (B, H)) / 8.0).astype(np.float32)  # exact in bf16 too
+    w2 = np.zeros((K, V, H), np.float32)
+    for k in range(K):
+        w2[k, np.arange(V), rhos[k]] = 1.0
+    def w1(sign):
+        a = np.zeros((K, H, H), np.float32)
+        for k in range(K):
+            a[k, np.arange(H), pis[k]] = sign
+        return a
+    return h, w1, w2, pis, rhos
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_silu_odd_part_pins_w1_orientation_and_heads(dtype):
+    # SiLU(x) - SiLU(-x) = x sigma(x) + x sigma(-x) = x for every x.  With
+    # W1_k = +P_k and W1_k = -P_k (b1 = 0) the two z's differ by exactly
+    # h[pi_k]; through the one-hot W2_k the logits differ by h[pi_k[rho_k(v)]].
+    # A transposed W1 would give h[pi_k^-1], a head offset another pi, a dropped
+    # residual or SiLU term a difference other than x.
+    h, w1, w2, pis, rhos = _perm_case(11)
+    K, H = w2.shape[0], h.shape[1]
+    b1 = np.zeros((K, H), np.float32)
+    conv = (lambda a: W.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    lp = O.heads_logits(conv(h), conv(w1(1.0)), conv(b1), conv(w2), dtype)
+    lm = O.heads_logits(conv(h), conv(w1(-1.0)), conv(b1), conv(w2), dtype)
+    for k in range(K):
+        np.testing.assert_allclose(lp[:, k] - lm[:, k], h[:, pis[k][rhos[k]]].astype(np.float64),
+                                   rtol=0, atol=1e-12)
+
+
+def test_silu_even_part_pins_the_sigmoid():
+    # SiLU(x) + SiLU(-x) = x (sigma(x) - sigma(-x)) = x tanh(x / 2), so the two
+    # z's above sum to 2 h + h[pi] tanh(h[pi] / 2).  The odd part alone cannot
+    # tell x sigma(x) from x sigma(-x); this sum changes sign between them.
+    h, w1, w2, pis, rhos = _perm_case(12)
+    K, H = w2.shape[0], h.shape[1]
+    b1 = np.zeros((K, H), np.float32)
+    lp = O.heads_logits(h, w1(1.0), b1, w2, "f32")
+    lm = O.heads_logits(h, w1(-1.0), b1, w2, "f32")
+    hd = h.astype(np.float64)
+    for k in range(K):
+        x = hd[:, pis[k]]
+        want = 2.0 * hd + x * np.tanh(x / 2.0)
+        np.testing.assert_allclose(lp[:, k] + lm[:, k], want[:, rhos[k]], rtol=0, atol=1e-12)
+
+
+def test_bias_odd_part_pins_bias_orientation():
+    # W1 = 0 and b1 = +c vs -c: z differs by exactly c_k (the bias of head k,
+    # feature i), whatever h is; through one-hot W2_k rows that is c_k[rho_k(v)].
+    h, _, w2, _, rhos = _perm_case(13)
+    K, H = w2.shape[0], h.shape[1]
+    rng = np.random.default_rng(14)
+    c = (rng.integers(-40, 41, (K, H)) / 16.0).astype(np.float32)
+    w1 = np.zeros((K, H, H), np.float32)
+    lp = O.heads_logits(h, w1, c, w2, "f32")
+    lm = O.heads_logits(h, w1, -c, w2, "f32")
+    for k in range(K):
+        np.testing.assert_allclose(lp[:, k] - lm[:, k], np.broadcast_to(c[k, rhos[k]], lp[:, k].shape),
+                                   rtol=0, atol=1e-12)
