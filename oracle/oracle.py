@@ -91,6 +91,18 @@ def lm_head_logits(h, lm, dtype):
     return out
 
 
+def lm_head_logits_matmul(h, lm, dtype):
+    """lm_head . h for many rows at once: the same definition as lm_head_logits
+    (bf16 decoded exactly, float64 arithmetic), with one float64 matrix product
+    of the library (numpy) as the step, for row counts the C loop would take
+    minutes over (e.g. 1364 tree rows x vocab 32000 x hidden 4096)."""
+    def dec(a):
+        if dtype == "f32":
+            return np.asarray(a, np.float32).astype(np.float64)
+        return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return dec(h) @ dec(lm).T
+
+
 def topk(x, k):
     """Top-k of each row of x (float64): (idx int32, val float64), sorted."""
     x = _c(x, np.float64)

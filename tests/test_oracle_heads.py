@@ -176,3 +176,16 @@ def test_bias_odd_part_pins_bias_orientation():
     for k in range(K):
         np.testing.assert_allclose(lp[:, k] - lm[:, k], np.broadcast_to(c[k, rhos[k]], lp[:, k].shape),
                                    rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_lm_head_matmul_form_equals_the_loop(dtype):
+    # the matrix-product form of the lm_head logits (for large row counts) gives
+    # the C loop's float64 values on shapes with ragged sizes
+    rng = np.random.default_rng(6)
+    h = rng.standard_normal((7, 40)).astype(np.float32)
+    lm = (rng.standard_normal((53, 40)) * 0.1).astype(np.float32)
+    conv = (lambda a: W.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    a = O.lm_head_logits(conv(h), conv(lm), dtype)
+    b = O.lm_head_logits_matmul(conv(h), conv(lm), dtype)
+    np.testing.assert_allclose(b, a, rtol=1e-13, atol=1e-13)

@@ -6,7 +6,7 @@ import torch
 
 import workloads as W
 from oracle import oracle as O
-from util import to_dev, to_np
+from util import oracle_attention_all, pool_map, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +54,7 @@ def test_attention_full_compare(medusa, kind, B, Hq, Hkv, D, lens, Lmax, dtype):
     kv_len = np.array(lens, np.int32)
     scale = float(np.float32(1 / np.sqrt(D)))
     got = _run(medusa, x, kv_len, t, scale)
-    ref = O.tree_attention(x["q"], x["k_cache"], x["v_cache"], kv_len, t["mask"], dtype, scale)
+    ref = oracle_attention_all(x["q"], x["k_cache"], x["v_cache"], kv_len, t["mask"], dtype, scale)
     assert np.abs(got - ref).max() <= TOL
 
 
@@ -73,7 +73,7 @@ def test_attention_many_blocks(medusa, kind, B, Hq, Hkv, D, lens, Lmax):
     kv_len = np.array(lens, np.int32)
     scale = float(np.float32(1 / np.sqrt(D)))
     got = _run(medusa, x, kv_len, t, scale)
-    ref = O.tree_attention(x["q"], x["k_cache"], x["v_cache"], kv_len, t["mask"], "bf16", scale)
+    ref = oracle_attention_all(x["q"], x["k_cache"], x["v_cache"], kv_len, t["mask"], "bf16", scale)
     assert np.abs(got - ref).max() <= TOL
 
 
@@ -85,9 +85,22 @@ def _sample_rows(B, N, Hq, n, seed):
     return rows.astype(np.int32)
 
 
+def _full_size_rows(c, N, seed):
+    """Rows compared at a workload's full size: at batch 1 every (node, query
+    head); at larger batches every query row of one query head per sequence
+    (the head rotating with the sequence, so all its KV-split CTAs and query
+    blocks are met), plus 96 random rows and the first and last row."""
+    B, Hq = c["B"], c["Hq"]
+    if B == 1:
+        n, h = np.meshgrid(np.arange(N), np.arange(Hq), indexing="ij")
+        return np.stack([np.zeros(N * Hq, int), n.ravel(), h.ravel()], 1).astype(np.int32)
+    full = [[b, i, (7 * b + 3) % Hq] for b in range(B) for i in range(N)]
+    return np.concatenate([np.array(full, np.int32), _sample_rows(B, N, Hq, 96, seed)], 0)
+
+
 @pytest.mark.parametrize("name,kind", [("h4096_b1_sparse64", "sparse64"), ("h5120_b8_ragged", "sparse64"),
                                        ("h4096_b4_kv8192", "dense"), ("h4096_b4_kv8192", "sparse64")])
-def test_attention_full_size_sampled(medusa, name, kind):
+def test_attention_full_size(medusa, name, kind):
     c = W.WORKLOADS[name]
     seed = c["seed"]
     t = _tree(kind)
@@ -98,9 +111,10 @@ def test_attention_full_size_sampled(medusa, name, kind):
                            dtype=c["dtype"])
     scale = float(np.float32(1 / np.sqrt(c["D"])))
     got = _run(medusa, x, kv_len, t, scale)
-    rows = _sample_rows(c["B"], N, c["Hq"], 96, seed=seed)
-    ref = O.tree_attention(x["q"], x["k_cache"], x["v_cache"], kv_len, t["mask"], c["dtype"], scale,
-                           rows=rows)
+    rows = _full_size_rows(c, N, seed)
+    chunks = np.array_split(rows, 32)
+    ref = np.concatenate(pool_map(lambda r: O.tree_attention(x["q"], x["k_cache"], x["v_cache"], kv_len,
+                                                             t["mask"], c["dtype"], scale, rows=r), chunks), 0)
     sel = got[rows[:, 0], rows[:, 1], rows[:, 2]]
     assert np.abs(sel - ref).max() <= TOL
     assert np.isfinite(got).all()
