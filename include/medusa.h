@@ -48,7 +48,8 @@ typedef enum {
     MEDUSA_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad alignment   */
     MEDUSA_ERR_UNSUPPORTED = -2, /* shape or dtype outside the supported limits  */
     MEDUSA_ERR_WORKSPACE = -3,   /* ws NULL or ws_bytes below the query's value  */
-    MEDUSA_ERR_CUDA = -4         /* a CUDA call or kernel launch failed          */
+    MEDUSA_ERR_CUDA = -4,        /* a CUDA call or kernel launch failed          */
+    MEDUSA_ERR_TIMEOUT = -5      /* a bounded device wait gave up (see below)    */
 } medusa_status;
 
 typedef enum { MEDUSA_F32 = 0, MEDUSA_BF16 = 1 } medusa_dtype;
@@ -59,6 +60,29 @@ const char* medusa_last_error(void);
 
 /* ABI version of this header (incremented on incompatible changes). */
 int medusa_abi_version(void);
+
+/* Device status of the tensor-core kernels (heads at bf16 batches 3-64, bf16
+ * tree attention, the fused verification projection).  Their mbarrier waits
+ * are bounded (about one second each).  A kernel whose wait gives up lets its
+ * own copies and MMAs in flight complete, frees its tensor memory, marks the
+ * outputs it owns (NaN attention rows, -1 top-k entries or -1 acceptance
+ * outputs) and sets a status word on the device.  No kernel traps.
+ *
+ * medusa_device_status synchronises `stream`, then reads and clears the
+ * current device's status words.  It returns MEDUSA_ERR_TIMEOUT if any wait on
+ * that device gave up since the previous check (whatever stream the call was
+ * on), MEDUSA_ERR_CUDA if the stream reported an error, MEDUSA_OK otherwise.
+ * Unlike the other entry points it blocks the calling host thread. */
+int medusa_device_status(void* stream);
+
+/* Test hook: sets, on the current device, the limit in SM clock cycles of the
+ * first waits of the tensor-core kernels (the waits for input tiles, MMA
+ * results and free buffers); cycles <= 0 restores the default (2^31, about
+ * one second).  The waits that let a giving-up kernel's copies and MMAs in
+ * flight complete keep the default limit.  A limit of a few cycles makes the
+ * waits run out on purpose, to exercise the path above.  Synchronous with
+ * respect to the host; do not call it while kernels of the library run. */
+int medusa_set_wait_limit(long long cycles);
 
 /* ------------------------------------------------------------------------- */
 /* 1. Medusa heads + per-head top-k  [MH, "How heads predict later tokens"]   */

@@ -16,10 +16,12 @@ the C ABI of include/medusa.h); this package is its thin Python binding:
                       on the tensor cores, reduced without writing the logits
   verify_accept_chain speculative-sampling acceptance with k + 1 tokens
   kv_compact          keep the accepted branch's KV rows and hidden state
+  device_status       raises if a bounded device wait gave up (MEDUSA_ERR_TIMEOUT)
+  set_wait_limit      test hook: the tensor-core kernels' wait limit
 """
 from ._native import MedusaError, lib  # noqa: F401
-from .api import (build_tree, heads_topk, heads_topk_static, heads_topk_workspace,  # noqa: F401
-                  kv_compact,
+from .api import (build_tree, device_status, heads_topk, heads_topk_static, heads_topk_workspace,  # noqa: F401
+                  kv_compact, set_wait_limit,
                   sparse_tree_paths, tree_attention, tree_attention_workspace, tree_layout,
                   verify_accept_chain, verify_accept_tree, verify_accept_workspace,
                   verify_accept_tree_sample, verify_chain_workspace, verify_project_tree,

@@ -12,11 +12,12 @@ import os
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmedusa_gb300.so")
 
 MEDUSA_F32, MEDUSA_BF16 = 0, 1
+MEDUSA_ERR_TIMEOUT = -5
 GREEDY, TYPICAL = 0, 1
 
 # every symbol include/medusa.h declares
 EXPORTS = (
-    "medusa_last_error", "medusa_abi_version",
+    "medusa_last_error", "medusa_abi_version", "medusa_device_status", "medusa_set_wait_limit",
     "medusa_heads_topk_workspace", "medusa_heads_topk", "medusa_heads_topk_static",
     "medusa_sparse_tree_paths", "medusa_tree_layout", "medusa_build_tree",
     "medusa_tree_attention_workspace", "medusa_tree_attention",
@@ -47,6 +48,8 @@ def lib() -> C.CDLL:
     P, i32, u64, f32, f64, sz = C.c_void_p, C.c_int, C.c_uint64, C.c_float, C.c_double, C.c_size_t
     L.medusa_last_error.restype = C.c_char_p
     L.medusa_abi_version.restype = i32
+    L.medusa_device_status.argtypes = [P]
+    L.medusa_set_wait_limit.argtypes = [C.c_longlong]
     L.medusa_heads_topk_workspace.argtypes = [i32] * 5
     L.medusa_heads_topk_workspace.restype = sz
     L.medusa_heads_topk.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P, P, sz, P]

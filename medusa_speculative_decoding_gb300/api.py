@@ -49,6 +49,20 @@ def _ws(nbytes, device):
 
 
 # ----------------------------------------------------------------------------
+def device_status(stream=None):
+    """Synchronises the stream and raises MedusaError (code MEDUSA_ERR_TIMEOUT,
+    -5) if a bounded wait of a tensor-core kernel on this device gave up since
+    the previous check; returns None otherwise."""
+    check(lib().medusa_device_status(_stream(stream)))
+
+
+def set_wait_limit(cycles):
+    """Test hook: limit (SM clock cycles) of the tensor-core kernels' first
+    waits on the current device; cycles <= 0 restores the default."""
+    check(lib().medusa_set_wait_limit(int(cycles)))
+
+
+# ----------------------------------------------------------------------------
 def heads_topk_workspace(B, K, H, V, topk):
     return int(lib().medusa_heads_topk_workspace(B, K, H, V, topk))
 

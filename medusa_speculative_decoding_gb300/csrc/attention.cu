@@ -28,6 +28,8 @@
 namespace medusa {
 namespace {
 
+MEDUSA_WAIT_CONTROL()
+
 constexpr int kBlockN = 128;  // keys per tile
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -105,7 +107,7 @@ constexpr int kAttnThreads = kSoftmaxThreads + 64;
 constexpr int kRing = 2;       // K and V ring depth
 constexpr int kMaxSplits = 8;  // portable cluster size
 constexpr float kRescaleThreshold = 8.f;
-constexpr long long kWaitCycles = 1ll << 31;  // ~1 s at 2 GHz
+constexpr long long kWaitCycles = kDefaultWaitCycles;  // drain waits (~1 s at 2 GHz)
 
 template <int D>
 struct AttnSmem {
@@ -115,8 +117,9 @@ struct AttnSmem {
     static constexpr int kOffV = kOffK + kRing * kTile;
     static constexpr int kOffRed = kOffV + kRing * kTile;     // float [2][4][128]
     static constexpr int kOffBar = kOffRed + 2 * 4 * 128 * 4;
-    // kfull[4] vfull[4] kempty[4] vempty[4] s_full[2] o_done[2] p_full[2] qfull
-    static constexpr int kNumBar = 4 * kRing + 7;
+    // kfull[kRing] vfull[kRing] kempty[kRing] vempty[kRing] s_full[2] o_done[2]
+    // p_full[2] qfull drain
+    static constexpr int kNumBar = 4 * kRing + 8;
     static constexpr int kOffMisc = kOffBar + kNumBar * 8;    // tmem slot, flag
     // query blocks of <= 64 rows: a receive area of its own for the split
     // partials (O [slots][D], then (max, sum) [slots]), so partials can arrive
@@ -159,9 +162,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
     const uint32_t bar_a = base_a + L::kOffBar;
     const uint32_t kfull0 = bar_a, vfull0 = kfull0 + 8 * kRing, kempty0 = vfull0 + 8 * kRing,
                    vempty0 = kempty0 + 8 * kRing, s_full0 = vempty0 + 8 * kRing,
-                   o_done0 = s_full0 + 16, p_full0 = o_done0 + 16, qfull = p_full0 + 16;
+                   o_done0 = s_full0 + 16, p_full0 = o_done0 + 16, qfull = p_full0 + 16, drain = qfull + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kOffMisc);
     volatile int* flag = reinterpret_cast<volatile int*>(base + L::kOffMisc + 4);
+    // limit of the first waits (input tiles, MMA results, free buffers); the
+    // drain waits below keep kWaitCycles
+    const long long lim = g_wait_limit;
+    // loads the TMA lane has issued: Q, and the K and V tiles below these counts
+    bool q_issued = false;
+    int issued_k = 0, issued_v = 0;
 
     // Set-up that reads no input runs before the dependency wait, overlapping
     // the previous kernel: barriers, tensor-map prefetch, TMEM, and (batch 1)
@@ -239,6 +248,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
     if (warp == kTmaWarp && lane == 0) {
         // Q and the first K/V tiles, while the softmax warps set up
         if (a.q_tma && ntiles > 0) {  // Q rows (node, group member) x D
+            q_issued = true;
             if (spread) {  // block rows 16g .. 16g+15 -> TMEM lanes 32g .. 32g+15
                 mbar_expect_tx(qfull, 4 * 16 * D * 2);
 #pragma unroll
@@ -255,6 +265,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
             }
         }
         for (int t = 0; t < kRing && t < ntiles; ++t) {
+            issued_k = issued_v = t + 1;
             mbar_expect_tx(kfull0 + 8 * t, L::kTile);
             mbar_expect_tx(vfull0 + 8 * t, L::kTile);
 #pragma unroll
@@ -300,7 +311,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
             bool fail = false;
             auto wait = [&](uint32_t bar, uint32_t parity) {
                 if (fail) return false;
-                if (!mbar_wait(bar, parity, kWaitCycles)) { fail = true; *flag = 1; return false; }
+                if (!mbar_wait(bar, parity, lim)) { fail = true; *flag = 1; return false; }
                 return true;
             };
             auto issue_s = [&](int t) {  // S_t = Q K_t^T into S buffer t & 1
@@ -343,38 +354,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
         }
     } else if (warp == kTmaWarp) {
         // -------------------------------- TMA lane --------------------------------
+        // (a CTA that gives up lets the loads issued here land after the
+        // block-wide barrier below, before it frees TMEM and leaves)
         if (lane == 0) {
-            int issued = min(kRing, ntiles);  // tiles whose K and V were requested
-            bool fail = false;
             for (int t = kRing; t < ntiles; ++t) {
                 // stage t % kRing held tile t - kRing: wait for the MMAs that read it
                 const uint32_t par = (uint32_t)((t / kRing - 1) & 1);
-                if (!mbar_wait(kempty0 + 8 * (t % kRing), par, kWaitCycles)) { fail = true; break; }
+                if (!mbar_wait(kempty0 + 8 * (t % kRing), par, lim)) { *flag = 1; break; }
                 mbar_expect_tx(kfull0 + 8 * (t % kRing), L::kTile);
 #pragma unroll
                 for (int x = 0; x < D / 64; ++x)
                     tma_load_3d(ks_a + (t % kRing) * L::kTile + x * kBlockN * 128, &tmk, x * 64, tile_start(t),
                                 zrow, kfull0 + 8 * (t % kRing));
-                if (!mbar_wait(vempty0 + 8 * (t % kRing), par, kWaitCycles)) {
-                    // K of tile t is in flight: let it land before giving up
-                    mbar_wait(kfull0 + 8 * (t % kRing), (uint32_t)((t / kRing) & 1), kWaitCycles);
-                    fail = true;
-                    break;
-                }
+                issued_k = t + 1;
+                if (!mbar_wait(vempty0 + 8 * (t % kRing), par, lim)) { *flag = 1; break; }
                 mbar_expect_tx(vfull0 + 8 * (t % kRing), L::kTile);
 #pragma unroll
                 for (int x = 0; x < D / 64; ++x)
                     tma_load_3d(vs_a + (t % kRing) * L::kTile + x * kBlockN * 128, &tmv, x * 64, tile_start(t),
                                 zrow, vfull0 + 8 * (t % kRing));
-                issued = t + 1;
-            }
-            if (fail) {
-                *flag = 1;
-                // let the loads in flight land before the CTA can leave
-                for (int t = max(0, issued - kRing); t < issued; ++t) {
-                    mbar_wait(kfull0 + 8 * (t % kRing), (uint32_t)((t / kRing) & 1), kWaitCycles);
-                    mbar_wait(vfull0 + 8 * (t % kRing), (uint32_t)((t / kRing) & 1), kWaitCycles);
-                }
+                issued_v = t + 1;
             }
         }
     } else {
@@ -388,7 +387,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
         const uint64_t* mrow = a.mask + (size_t)node * a.W;
         bool fail = false;
         for (int j = 0; j < ntiles; ++j) {
-            bool ok = !fail && mbar_wait(s_full0 + 8 * (j & 1), (uint32_t)((j >> 1) & 1), kWaitCycles);
+            bool ok = !fail && mbar_wait(s_full0 + 8 * (j & 1), (uint32_t)((j >> 1) & 1), lim);
             ok = __all_sync(0xffffffffu, ok);
             fence_after_sync();
             float sv[SW];
@@ -439,7 +438,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
             l *= corr;
             if (warp_valid && __any_sync(0xffffffffu, rescale)) {
                 // O must hold PV_{j-1} before it is rescaled (warp-collective TMEM access)
-                ok = mbar_wait(o_done0 + 8 * ((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1), kWaitCycles);
+                ok = mbar_wait(o_done0 + 8 * ((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1), lim);
                 ok = __all_sync(0xffffffffu, ok);
                 fence_after_sync();
                 if (ok) {
@@ -489,7 +488,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
         }
         bool ok = !fail;
         if (ok && ntiles > 0)
-            ok = mbar_wait(o_done0 + 8 * ((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1), kWaitCycles);
+            ok = mbar_wait(o_done0 + 8 * ((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1), lim);
         float* rl = red + (ntiles & 1) * 4 * 128;
         rl[q * 128 + r] = l;
         bad = named_barrier_or(1, kSoftmaxThreads, !ok);
@@ -498,6 +497,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
     }
     bad = __syncthreads_or(bad);
     bad = bad || *flag != 0;  // every write to the flag precedes the barrier
+    if (bad) {
+        // Gave up: let everything this CTA started complete before its tensor
+        // memory is freed and it leaves (default-limit waits).  The MMA lane
+        // commits once more, which tracks every MMA it issued; the TMA lane
+        // waits for Q and for the last kRing K and V tiles it requested (older
+        // tiles completed before their stage was requested again).
+        if (warp == kMmaWarp && lane == 0) {
+            commit(drain);
+            mbar_wait(drain, 0, kWaitCycles);
+        }
+        if (warp == kTmaWarp && lane == 0) {
+            if (q_issued) mbar_wait(qfull, 0, kWaitCycles);
+            for (int t = max(0, issued_k - kRing); t < issued_k; ++t)
+                mbar_wait(kfull0 + 8 * (t % kRing), (uint32_t)((t / kRing) & 1), kWaitCycles);
+            for (int t = max(0, issued_v - kRing); t < issued_v; ++t)
+                mbar_wait(vfull0 + 8 * (t % kRing), (uint32_t)((t / kRing) & 1), kWaitCycles);
+        }
+        if (tid == 0) atomicExch(&g_wait_gave_up, 1);
+    }
 
     // ------------------------------ epilogue ------------------------------
     float ov[QW];

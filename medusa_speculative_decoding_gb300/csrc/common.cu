@@ -101,7 +101,68 @@ int current_context_id(unsigned long long* id) {
     return MEDUSA_OK;
 }
 
+namespace {
+struct WaitControl {
+    int (*read_clear)(int*, cudaStream_t);
+    int (*set_limit)(long long);
+};
+std::mutex g_wc_mu;
+// function-local statics: registration runs during static initialisation of
+// the other translation units, whose order is unspecified
+WaitControl* wait_controls(int*) {
+    static WaitControl tab[8];
+    return tab;
+}
+int& wait_control_count() {
+    static int count = 0;
+    return count;
+}
+}  // namespace
+
+void register_wait_control(int (*read_clear)(int*, cudaStream_t), int (*set_limit)(long long)) {
+    std::lock_guard<std::mutex> lk(g_wc_mu);
+    int& n = wait_control_count();
+    if (n < 8) wait_controls(nullptr)[n++] = WaitControl{read_clear, set_limit};
+}
+
+int wait_controls_read_clear(int* gave_up, cudaStream_t st) {
+    std::lock_guard<std::mutex> lk(g_wc_mu);
+    const int n = wait_control_count();
+    for (int i = 0; i < n; ++i) {
+        const int e = wait_controls(nullptr)[i].read_clear(gave_up, st);
+        if (e) return fail(MEDUSA_ERR_CUDA, "device status: %s", cudaGetErrorString((cudaError_t)e));
+    }
+    return MEDUSA_OK;
+}
+
+int wait_controls_set_limit(long long cycles) {
+    std::lock_guard<std::mutex> lk(g_wc_mu);
+    const int n = wait_control_count();
+    for (int i = 0; i < n; ++i) {
+        const int e = wait_controls(nullptr)[i].set_limit(cycles);
+        if (e) return fail(MEDUSA_ERR_CUDA, "set_wait_limit: %s", cudaGetErrorString((cudaError_t)e));
+    }
+    return MEDUSA_OK;
+}
+
 }  // namespace medusa
+
+extern "C" int medusa_device_status(void* stream) {
+    cudaStream_t st = medusa::as_stream(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return medusa::fail(MEDUSA_ERR_CUDA, "device_status: the stream failed: %s", cudaGetErrorString(e));
+    int gave_up = 0;
+    int rc = medusa::wait_controls_read_clear(&gave_up, st);
+    if (rc) return rc;
+    if (gave_up)
+        return medusa::fail(MEDUSA_ERR_TIMEOUT,
+                            "device_status: a bounded device wait gave up; the outputs of the calls it "
+                            "belonged to are marked (NaN or -1)");
+    return MEDUSA_OK;
+}
+
+extern "C" int medusa_set_wait_limit(long long cycles) { return medusa::wait_controls_set_limit(cycles); }
 
 extern "C" const char* medusa_last_error(void) { return medusa::g_msg; }
 extern "C" int medusa_abi_version(void) { return 1; }

@@ -21,6 +21,42 @@ int current_context_id(unsigned long long* id);
 // Opt-in maximum dynamic shared memory per block of the current device.
 int max_smem_optin();
 
+// ---------------------------------------------------------------------------
+// Bounded device waits.  Every mbarrier wait of the tensor-core kernels gives
+// up after a limit (about one second by default).  A kernel whose wait gave up
+// first lets its own copies and MMAs in flight complete (those drain waits keep
+// the default limit), frees its tensor memory, marks its outputs and sets the
+// give-up word of its translation unit; medusa_device_status() reads and
+// clears the words.  The limit of the first waits can be lowered through
+// medusa_set_wait_limit() (a test hook that makes the waits run out on
+// purpose).  Each .cu file with such kernels defines its own words with
+// MEDUSA_WAIT_CONTROL() and registers a reader and a setter here.
+constexpr long long kDefaultWaitCycles = 1ll << 31;  // ~1 s at 2 GHz
+void register_wait_control(int (*read_clear)(int* gave_up, cudaStream_t st), int (*set_limit)(long long cycles));
+int wait_controls_read_clear(int* gave_up, cudaStream_t st);
+int wait_controls_set_limit(long long cycles);
+
+#define MEDUSA_WAIT_CONTROL()                                                                              \
+    __device__ int g_wait_gave_up = 0;                                                                     \
+    __device__ long long g_wait_limit = ::medusa::kDefaultWaitCycles;                                      \
+    int wait_read_clear(int* gave_up, cudaStream_t st) {                                                   \
+        static const int zero = 0;                                                                         \
+        int v = 0;                                                                                         \
+        cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_wait_gave_up, sizeof v, 0, cudaMemcpyDeviceToHost, st); \
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);                                               \
+        if (e == cudaSuccess && v)                                                                         \
+            e = cudaMemcpyToSymbolAsync(g_wait_gave_up, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, st); \
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);                                               \
+        if (e != cudaSuccess) return (int)e;                                                               \
+        *gave_up = *gave_up || v != 0;                                                                     \
+        return 0;                                                                                          \
+    }                                                                                                      \
+    int wait_set_limit(long long cycles) {                                                                 \
+        const long long v = cycles > 0 ? cycles : ::medusa::kDefaultWaitCycles;                            \
+        return (int)cudaMemcpyToSymbol(g_wait_limit, &v, sizeof v);                                        \
+    }                                                                                                      \
+    const bool g_wait_registered = (::medusa::register_wait_control(wait_read_clear, wait_set_limit), true);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

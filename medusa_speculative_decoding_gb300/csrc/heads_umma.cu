@@ -23,8 +23,9 @@
 //   heads_merge_kernel   : merges every head's run lists into the sorted top-k
 // Roles of the two tensor-core kernels (192 threads): warp 0 TMA producer, warp
 // 1 TMEM allocation and MMA issue, warps 2-5 epilogue (warp w reads TMEM lanes
-// 32*(w%4) ..).  Every wait is bounded; a CTA that gives up marks the call's
-// status word, and the merge then writes -1 into every top-k list.
+// 32*(w%4) ..).  Every wait is bounded; every CTA writes its own status slot
+// (nonzero if a wait gave up), and the merge then writes -1 into every top-k
+// list of a call in which any slot is set.
 #include <float.h>
 #include <limits.h>
 
@@ -36,6 +37,8 @@
 namespace medusa {
 namespace {
 
+MEDUSA_WAIT_CONTROL()
+
 constexpr int kUM = 128;                 // weight rows per tile (MMA M)
 constexpr int kUK = 64;                  // hidden elements per stage
 constexpr int kUThreads = 192;
@@ -43,7 +46,7 @@ constexpr int kUA = kUM * kUK * 2;       // 16 KB of weight rows per stage
 constexpr int kUMinB = 3, kUMaxB = 64;    // batches on the tensor cores
 constexpr int kUTopk = 16;
 constexpr int kUSmemCap = 227 * 1024;    // opt-in shared memory per CTA
-constexpr long long kUWait = 1ll << 31;  // ~1 s at 2 GHz
+constexpr long long kUWait = kDefaultWaitCycles;  // drain waits (~1 s at 2 GHz)
 
 // ring of STAGES x (16 KB weights + BBYTES activations) | barriers | tmem slot,
 // flags | EXTRA bytes of epilogue staging.  Accumulator buffer i sits at TMEM
@@ -116,6 +119,8 @@ __device__ __forceinline__ bool umma_pipeline(uint8_t* base, uint32_t tmem, int 
     auto d_empty = [&](int i) { return bar0 + 8 * (2 * Sm::kStages + 2 + i); };
     const uint32_t drain = bar0 + 8 * (2 * Sm::kStages + 4);
     volatile int* fail_flag = reinterpret_cast<volatile int*>(base + Sm::kOffMisc + 4);
+    // limit of the first waits; the drain waits keep kUWait
+    const long long lim = g_wait_limit;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bbytes = (uint32_t)N * kUK * 2;
     int issued = 0;
@@ -127,7 +132,7 @@ __device__ __forceinline__ bool umma_pipeline(uint8_t* base, uint32_t tmem, int 
                 coords(it, ay, by);
                 for (int kb = 0; kb < nkb; ++kb, ++issued) {
                     const int st = issued % Sm::kStages;
-                    if (issued >= Sm::kStages && !mbar_wait(empty(st), ((issued / Sm::kStages) - 1) & 1, kUWait)) {
+                    if (issued >= Sm::kStages && !mbar_wait(empty(st), ((issued / Sm::kStages) - 1) & 1, lim)) {
                         ok = false;
                         break;
                     }
@@ -146,7 +151,7 @@ __device__ __forceinline__ bool umma_pipeline(uint8_t* base, uint32_t tmem, int 
             int it2 = 0;
             for (int it = 0; it < nitems && ok; ++it) {
                 const int buf = it & 1;
-                if (it >= 2 && !mbar_wait(d_empty(buf), ((it / 2) - 1) & 1, kUWait)) {
+                if (it >= 2 && !mbar_wait(d_empty(buf), ((it / 2) - 1) & 1, lim)) {
                     ok = false;
                     break;
                 }
@@ -154,7 +159,7 @@ __device__ __forceinline__ bool umma_pipeline(uint8_t* base, uint32_t tmem, int 
                 const uint32_t d = tmem + (uint32_t)(buf * Sm::kAcc);
                 for (int kb = 0; kb < nkb; ++kb, ++it2) {
                     const int st = it2 % Sm::kStages;
-                    if (!mbar_wait(full(st), (it2 / Sm::kStages) & 1, kUWait)) {
+                    if (!mbar_wait(full(st), (it2 / Sm::kStages) & 1, lim)) {
                         ok = false;
                         break;
                     }
@@ -176,7 +181,7 @@ __device__ __forceinline__ bool umma_pipeline(uint8_t* base, uint32_t tmem, int 
         bool ok = true;
         for (int it = 0; it < nitems; ++it) {
             const int buf = it & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(d_full(buf), (it / 2) & 1, kUWait));
+            ok = __all_sync(0xffffffffu, mbar_wait(d_full(buf), (it / 2) & 1, lim));
             if (!ok) break;
             fence_after_sync();
             epi(it, (uint32_t)(buf * Sm::kAcc));
@@ -192,6 +197,7 @@ __device__ __forceinline__ bool umma_pipeline(uint8_t* base, uint32_t tmem, int 
     if (failed && warp == 0 && lane == 0)  // let copies in flight land first
         for (int i = max(0, issued - Sm::kStages); i < issued; ++i)
             mbar_wait(full(i % Sm::kStages), (i / Sm::kStages) & 1, kUWait);
+    if (failed && threadIdx.x == 0) atomicExch(&g_wait_gave_up, 1);
     return !failed;
 }
 
@@ -239,7 +245,6 @@ __global__ void __launch_bounds__(kUThreads, 2) heads_w1_umma_kernel(
     uint32_t tmem;
     umma_setup<Sm>(base, &tmem);
     pdl_wait();  // h may come from the previous kernel (the last round's compaction)
-    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
     pdl_trigger();
     const int tiles = K * H / kUM;
     const int i0 = (int)((long long)blockIdx.x * tiles / gridDim.x);
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(kUThreads, 2) heads_w1_umma_kernel(
         }
     };
     const bool ok = umma_pipeline<Sm>(base, tmem, i1 - i0, H / kUK, N1, &tmw, &tmh, coords, epi);
-    if (!ok && threadIdx.x == 0) atomicExch(status, 1);
+    if (threadIdx.x == 0) status[blockIdx.x] = ok ? 0 : 1;  // this CTA's own slot: no race, no reset
     if (warp == 1) {
         fence_after_sync();
         tmem_dealloc(tmem, Sm::kTmemCols);
@@ -287,7 +292,9 @@ struct W2Args {
     float* logits;      // [B][K][V] or nullptr
     float* run_val;     // [K][grid][B][topk]
     int* run_idx;
-    int* status;
+    const int* status1;  // [n1]: one slot per CTA of the W1 kernel, nonzero if it gave up
+    int n1;
+    int* status2;        // [grid of the W2 kernel]: the same for the W2 kernel
     int32_t* topk_idx;  // [B][K][topk]
     float* topk_val;    // or nullptr
 };
@@ -466,11 +473,13 @@ __global__ void __launch_bounds__(kUThreads, 1) heads_w2_umma_kernel(
         named_barrier_or(1, kEpi, false);
     };
     // a failure of the first kernel leaves the z planes undefined
-    const bool ok1 = __syncthreads_or(*(volatile int*)a.status != 0) == 0;
+    int bad1 = 0;
+    for (int i = threadIdx.x; i < a.n1; i += blockDim.x) bad1 |= a.status1[i];
+    const bool ok1 = __syncthreads_or(bad1) == 0;
     bool ok = ok1 && umma_pipeline<Sm>(base, tmem, i1 - i0, a.H / kUK, Cfg::kN, &tmw, &tmz, coords, epi);
     if (ok && warp >= 2 && run_k >= 0) finish_run(run_k);
+    if (threadIdx.x == 0) a.status2[blockIdx.x] = ok ? 0 : 1;
     if (!ok) {
-        if (threadIdx.x == 0) atomicExch(a.status, 1);
         const int k0 = i0 / T, k1 = (i1 - 1) / T;
         const int n = (k1 - k0 + 1) * B * topk;
         for (int j = threadIdx.x; j < n; j += blockDim.x) {
@@ -495,7 +504,9 @@ __global__ void __launch_bounds__(128) heads_merge_kernel(W2Args a, int grid2) {
     const int k = w / a.B, b = w - (w / a.B) * a.B, topk = a.topk;
     int32_t* oi = a.topk_idx + ((size_t)b * a.K + k) * topk;
     float* ov = a.topk_val ? a.topk_val + ((size_t)b * a.K + k) * topk : nullptr;
-    if (*(volatile int*)a.status != 0) {
+    int bad = 0;
+    for (int i = lane; i < grid2; i += 32) bad |= a.status2[i];
+    if (__any_sync(0xffffffffu, bad != 0)) {
         if (lane < topk) oi[lane] = -1;
         return;
     }
@@ -561,7 +572,7 @@ size_t heads_umma_workspace(int B, int K, int H, int V, int topk) {
     size_t off = align_up((size_t)K * 3 * pad16(B) * H * 2, 256);      // z planes
     off = align_up(off + (size_t)K * grid * B * topk * 4, 256);            // run values
     off = align_up(off + (size_t)K * grid * B * topk * 4, 256);            // run indices
-    return align_up(off + 16, 256);                                        // status
+    return align_up(off + (size_t)3 * grid * 4, 256);                      // per-CTA status slots
 }
 
 template <int BP>
@@ -584,7 +595,7 @@ int launch_heads_umma(const void* h, const void* w1, const void* b1, const void*
     off = align_up(off + (size_t)K * grid * B * topk * 4, 256);
     int* run_idx = reinterpret_cast<int*>(ws + off);
     off = align_up(off + (size_t)K * grid * B * topk * 4, 256);
-    int* status = reinterpret_cast<int*>(ws + off);
+    int* status = reinterpret_cast<int*>(ws + off);  // W1 slots [0, g1), then W2 slots [g1, g1 + g2)
     CUtensorMap tw1, th, tw2, tz;
     int rc = bf16_rows_map(&tw1, w1, H, (long long)K * H, kUM);
     if (!rc) rc = bf16_rows_map(&th, h, H, B, Bp);
@@ -594,7 +605,8 @@ int launch_heads_umma(const void* h, const void* w1, const void* b1, const void*
     const int tiles1 = K * H / kUM;
     auto k1 = heads_w1_umma_kernel<W1Smem>;
     cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, W1Smem::kBytes);
-    cudaError_t e = launch(k1, dim3(min(2 * grid, tiles1)), dim3(kUThreads), (size_t)W1Smem::kBytes, st, tw1, th,
+    const int g1 = min(2 * grid, tiles1);
+    cudaError_t e = launch(k1, dim3(g1), dim3(kUThreads), (size_t)W1Smem::kBytes, st, tw1, th,
                            static_cast<const uint16_t*>(h), static_cast<const uint16_t*>(b1), B, K, H, Bp, Bp, zp,
                            status);
     if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "heads_w1_umma: launch failed: %s", cudaGetErrorString(e));
@@ -604,7 +616,9 @@ int launch_heads_umma(const void* h, const void* w1, const void* b1, const void*
     a.logits = logits;
     a.run_val = run_val;
     a.run_idx = run_idx;
-    a.status = status;
+    a.status1 = status;
+    a.n1 = g1;
+    a.status2 = status + g1;
     a.topk_idx = topk_idx;
     a.topk_val = topk_val;
     const int g2 = min(grid, a.items);

@@ -37,6 +37,8 @@
 namespace medusa {
 namespace {
 
+MEDUSA_WAIT_CONTROL()
+
 constexpr int kPM = 128;      // tree rows per block (MMA M)
 constexpr int kPN = 256;      // largest vocab tile (MMA N); the plan picks 128..256
 constexpr int kPK = 64;       // hidden elements per stage (one 128-byte swizzle span)
@@ -47,7 +49,7 @@ constexpr int kPB = kPN * kPK * 2;  // 32 KB of lm_head rows per stage
 constexpr int kPStage = kPA + kPB;
 constexpr int kPBars = 2 * kPStages + 2 + 2 + 1;  // full, empty, d_full, d_empty, drain
 constexpr int kPSmem = kPStages * kPStage + kPBars * 8 + 16 + 1024;
-constexpr long long kPWait = 1ll << 31;  // ~1 s at 2 GHz
+constexpr long long kPWait = kDefaultWaitCycles;  // drain waits (~1 s at 2 GHz)
 
 struct ProjArgs {
     int rows;        // B * N
@@ -80,6 +82,8 @@ __global__ void __launch_bounds__(kPThreads, 1) project_stats_kernel(
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int s = blockIdx.x, nb = blockIdx.y;
+    // limit of the first waits; the drain waits keep kPWait
+    const long long lim = g_wait_limit;
     const int t0 = (int)((long long)s * a.tiles / a.splits);
     const int t1 = (int)((long long)(s + 1) * a.tiles / a.splits);
     const int ntiles = t1 - t0;
@@ -113,7 +117,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_stats_kernel(
                 for (int kb = 0; kb < a.nkb; ++kb, ++issued) {
                     const int st = issued % kPStages;
                     if (issued >= kPStages &&
-                        !mbar_wait(empty(st), ((issued / kPStages) - 1) & 1, kPWait)) {
+                        !mbar_wait(empty(st), ((issued / kPStages) - 1) & 1, lim)) {
                         ok = false;
                         break;
                     }
@@ -131,7 +135,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_stats_kernel(
             int it = 0;
             for (int tl = 0; tl < ntiles && ok; ++tl) {
                 const int buf = tl & 1;
-                if (tl >= 2 && !mbar_wait(d_empty(buf), ((tl / 2) - 1) & 1, kPWait)) {
+                if (tl >= 2 && !mbar_wait(d_empty(buf), ((tl / 2) - 1) & 1, lim)) {
                     ok = false;
                     break;
                 }
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_stats_kernel(
                 const uint32_t d = tmem + (uint32_t)(buf * kPN);
                 for (int kb = 0; kb < a.nkb; ++kb, ++it) {
                     const int st = it % kPStages;
-                    if (!mbar_wait(full(st), (it / kPStages) & 1, kPWait)) {
+                    if (!mbar_wait(full(st), (it / kPStages) & 1, lim)) {
                         ok = false;
                         break;
                     }
@@ -170,7 +174,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_stats_kernel(
         bool ok = true;
         for (int tl = 0; tl < ntiles; ++tl) {
             const int buf = tl & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(d_full(buf), (tl / 2) & 1, kPWait));
+            ok = __all_sync(0xffffffffu, mbar_wait(d_full(buf), (tl / 2) & 1, lim));
             if (!ok) break;
             fence_after_sync();
             const int v0 = (t0 + tl) * a.tn;
@@ -245,6 +249,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_stats_kernel(
             mbar_wait(full(i % kPStages), (i / kPStages) & 1, kPWait);
     }
     if (threadIdx.x == 0) a.status[(size_t)nb * a.splits + s] = failed ? 1 : 0;
+    if (failed && threadIdx.x == 0) atomicExch(&g_wait_gave_up, 1);
     if (warp == 1) {
         fence_after_sync();
         tmem_dealloc(tmem, 2 * kPN);

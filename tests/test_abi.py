@@ -119,3 +119,15 @@ def test_product_path_has_no_cpu_fallback():
     from medusa_speculative_decoding_gb300 import api
     src = open(api.__file__).read()
     assert "oracle" not in src and "numpy.linalg" not in src
+
+
+def test_device_status_calls_report_a_missing_device(M):
+    # medusa_device_status / medusa_set_wait_limit touch the device; without one
+    # they return MEDUSA_ERR_CUDA with a message instead of crashing
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present: tests/test_parity_timeout.py covers these calls")
+    L = M.lib()
+    assert L.medusa_device_status(None) == -4
+    assert L.medusa_last_error()
+    assert L.medusa_set_wait_limit(5) == -4
