@@ -12,20 +12,29 @@ with every input resident in HBM.  The step reads ~1.52 GB, more than L2, so
 consecutive steps start cold.  kv_len is restored before each step (compaction
 grows it) so every step sees the same workload.
 
-Beside the step, the JSON line carries "step_graph_32_layers" (the step as one
-CUDA graph with tree attention over 32 layers' caches), "attention_workloads" (tree attention
-alone at the batch-8 ragged and batch-4 KV-8192 shapes), "chain_acceptance"
-(speculative-sampling acceptance at batch 64, vocab 128256), "heads_batches"
-(a batch sweep of the heads alone: batch 1-64 at hidden 4096, batch 8 at
-hidden 5120), "tree_sizes" (the step with the sparse 64-node and the dense
-341-node tree at equal planted acceptance) and
-"verify_projection": the fused
-verification projection (lm_head x tree hidden states on the tensor cores,
-reduced to acceptance without writing logits) timed at the step's shapes and at
-batch 4 of the dense 341-node tree.
+Beside the step, the JSON line carries:
+  step_graph_32_layers  the step as one CUDA graph with tree attention over 32
+                        layers' caches, and the per-layer attention time
+  chained_rounds        16 chained rounds as one CUDA graph (root = the last
+                        next token, heads on h_next, kv_len growing), with 1 and
+                        32 attention layers: tokens per wall-second
+  tree_sizes            the step with the sparse 64-node and the dense 341-node
+                        tree at equal planted acceptance
+  workload_steps        whole steps of the 13B-shaped ragged batch-8 workload and
+                        of the batch-4 KV-8192 workload (sparse and dense tree,
+                        typical acceptance): steps/s and tree tokens/s
+  verify_projection     the fused verification projection (lm_head x tree
+                        hidden states on the tensor cores, reduced to acceptance)
+  attention_workloads   tree attention alone at the batched shapes
+  chain_sweep           speculative-sampling acceptance at batch 64, vocab
+                        128256, sigma 0.1/0.5/1.0 x gamma 0..32, 64 rounds each:
+                        measured alpha and tokens per round against E
+  chain_acceptance      that call's HBM roofline at gamma 1/4/8/32
+  heads_batches         the heads alone at batch 1-64
+  cpu_baseline          the float64 C oracle on the host cores
 
-Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
-bounded sample of the same step instead.
+Prints one JSON line (rank 0).  --impl reference runs the oracle's full step
+instead: --warmup then --steps steps, spread over the host cores.
 """
 from __future__ import annotations
 
@@ -654,109 +663,443 @@ def measure_heads_batches(dev, iters=10, warmup=2):
     return out
 
 
-def measure_chain(dev, gammas=(1, 4, 8, 32), sigma=0.5, reps=10):
-    """medusa_verify_accept_chain at batch 64, vocab 128256 (the speculative-
-    sampling sweep's shape): q = softmax(ql), p = softmax(ql + N(0, sigma)),
-    ql ~ N(0, 2), drafts drawn from q; L2 is flushed (a 512 MB write) before
-    every timed call, and each call is timed alone with events.  Algorithmic
-    bytes: the gathered p and q entries of the drafts examined, plus the row the
-    draw reads (p and q at a rejection, 8V bytes; p alone for a bonus, 4V)."""
+# ----------------------------------------------------------------------------
+# whole decode steps of the batched workloads
+# ----------------------------------------------------------------------------
+DENSE_PATHS = np.array([[a, b, x, y] for a in range(4) for b in range(4) for x in range(4) for y in range(4)],
+                       np.int32)
+
+
+class WorkloadStep:
+    """The five C-ABI calls of one decode step of a batched workload, with
+    random-init weights of its shape drawn on the GPU (seeded), the workload's
+    KV lengths, and verifier logits planted around the step's own candidates
+    (greedy, alpha = 0.8) or drawn N(0, 3) (typical acceptance)."""
+
+    def __init__(self, name, tree_kind, dev, seed=21):
+        import torch
+        import medusa_speculative_decoding_gb300 as M
+        self.M, self.torch, self.name = M, torch, name
+        c = self.c = W.WORKLOADS[name]
+        paths, md = ((M.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5) if tree_kind == "sparse64" else (DENSE_PATHS, 4))
+        t = self.t = M.tree_layout(paths, md)
+        self.N, self.Dmax = t["N"], t["max_depth"]
+        B, H, V, K, topk = c["B"], c["H"], c["V"], c["K"], c["topk"]
+        Hq, Hkv, D = c["Hq"], c["Hkv"], c["D"]
+        self.mode = "typical" if c["accept"] == "typical" else "greedy"
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        bf = torch.bfloat16
+        rn = lambda *shape, std=1.0: (torch.randn(*shape, device=dev, generator=g) * std).to(bf)
+        self.h = rn(B, H)
+        self.w1 = rn(K, H, H, std=c["w_std"])
+        self.b1 = torch.zeros(K, H, device=dev, dtype=bf)
+        self.w2 = rn(K, V, H, std=c["w_std"])
+        self.kv_len0 = torch.from_numpy(W.kv_lengths(c["seed"], B, c["L_lo"], c["L_hi"])).to(dev)
+        self.kv_len = self.kv_len0.clone()
+        Lmax = c["L_hi"] + self.N
+        self.q = rn(B, self.N, Hq, D)
+        self.kc, self.vc = rn(B, Hkv, Lmax, D), rn(B, Hkv, Lmax, D)
+        self.ht = rn(B, self.N, H)
+        self.scale = 1.0 / float(np.sqrt(D))
+        td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        self.root = td(W.root_tokens(c["seed"], B, V))
+        self.depth, self.rank, self.parent = td(t["depth"]), td(t["rank"]), td(t["parent"])
+        self.mask = torch.from_numpy(t["mask"].view(np.int64)).to(dev)
+        i32 = torch.int32
+        self.idx = torch.empty(B, K, topk, dtype=i32, device=dev)
+        self.val = torch.empty(B, K, topk, device=dev)
+        self.cand = torch.empty(B, self.N, dtype=i32, device=dev)
+        self.att_out = torch.empty(B, self.N, Hq, D, device=dev)
+        self.acc = dict(accept_len=torch.empty(B, dtype=i32, device=dev), best_node=torch.empty(B, dtype=i32, device=dev),
+                        path_nodes=torch.empty(B, self.Dmax + 1, dtype=i32, device=dev),
+                        next_tok=torch.empty(B, dtype=i32, device=dev))
+        self.h_next = torch.empty(B, H, dtype=bf, device=dev)
+        self.src = torch.empty(B, self.Dmax + 1, dtype=i32, device=dev)
+        u8 = torch.uint8
+        self.ws_heads = torch.empty(max(16, M.heads_topk_workspace(B, K, H, V, topk)), dtype=u8, device=dev)
+        self.ws_att = torch.empty(max(16, M.tree_attention_workspace(B, self.N, Hq, Hkv, D, Lmax)), dtype=u8,
+                                  device=dev)
+        self.ws_ver = torch.empty(max(16, M.verify_accept_workspace(B, self.N, V)), dtype=u8, device=dev)
+        self.heads()
+        M.build_tree(self.idx, self.root, self.depth, self.rank, out=self.cand)
+        if self.mode == "greedy":
+            self.vlogits = td(W.planted_logits(c["seed"], self.cand.cpu().numpy(), t["parent"], V, c["alpha"]))
+        else:
+            self.vlogits = torch.randn(B, self.N, V, device=dev, generator=g) * float(c["logit_std"])
+        lens = self.kv_len0.cpu().numpy()
+        self.bytes = {
+            "heads": K * (H * H + H + V * H) * 2 + B * H * 2 + B * K * topk * 8,
+            "attention": sum(2 * Hkv * (int(L) + self.N) * D * 2 for L in lens) + B * self.N * Hq * D * (2 + 4),
+            "verify": B * self.N * V * 4 + B * self.N * 4}
+
+    def heads(self):
+        self.M.heads_topk(self.h, self.w1, self.b1, self.w2, self.c["topk"], out=(self.idx, self.val, None),
+                          ws=self.ws_heads)
+
+    def run(self, ev=None):
+        M = self.M
+        rec = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
+        self.kv_len.copy_(self.kv_len0)
+        rec(0)
+        self.heads()
+        rec(1)
+        M.build_tree(self.idx, self.root, self.depth, self.rank, out=self.cand)
+        rec(2)
+        M.tree_attention(self.q, self.kc, self.vc, self.kv_len, self.mask, self.scale, out=self.att_out,
+                         ws=self.ws_att)
+        rec(3)
+        M.verify_accept_tree(self.vlogits, self.cand, self.parent, self.depth, self.Dmax, self.mode,
+                             out=self.acc, ws=self.ws_ver)
+        rec(4)
+        M.kv_compact(self.kc, self.vc, self.kv_len, self.acc["path_nodes"], self.acc["accept_len"],
+                     self.acc["best_node"], self.N, self.Dmax, hidden_tree=self.ht, h_next=self.h_next,
+                     src_idx=self.src)
+        rec(5)
+
+
+def measure_workload_steps(dev, iters=100, warmup=10):
+    """Whole decode steps (heads -> tree -> tree attention, one layer ->
+    acceptance -> compaction) of the 13B-shaped ragged batch-8 workload (sparse
+    64-node tree, greedy) and the batch-4 KV-8192 workload with the sparse
+    64-node and the dense 341-node tree (typical acceptance): steps/s, tree
+    tokens verified/s, per-call times, and the step's algorithmic bytes against
+    the HBM ceiling.  `iters` back-to-back steps with events at the two ends
+    (each step streams 1.9-2.3 GB, more than L2); a second pass with events
+    around every call gives the per-call times."""
+    import torch
+    hbm, kind = _peaks()
+    out = {}
+    for key, name, tree in (("h5120_b8_ragged_sparse64_greedy", "h5120_b8_ragged", "sparse64"),
+                            ("h4096_b4_kv8192_sparse64_typical", "h4096_b4_kv8192", "sparse64"),
+                            ("h4096_b4_kv8192_dense341_typical", "h4096_b4_kv8192", "dense341")):
+        s = WorkloadStep(name, tree, dev)
+        for _ in range(warmup):
+            s.run()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            s.run()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / iters
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(20)]
+        for e in evs:
+            s.run(e)
+        torch.cuda.synchronize()
+        calls = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) * 1e3 for e in evs) for i, n in enumerate(Step.CALLS)}
+        total = sum(s.bytes.values())
+        B = s.c["B"]
+        out[key] = {"batch": B, "nodes": s.N, "acceptance": s.mode, "us_per_step": us, "steps_per_s": 1e6 / us,
+                    "tree_tokens_verified_per_s": B * s.N * 1e6 / us,
+                    "tokens_per_step": float((s.acc["accept_len"].float() + 1).sum().item()),
+                    "call_us": {k: round(v, 2) for k, v in calls.items()},
+                    "algorithmic_bytes": s.bytes, "step_gbs": total / (us * 1e-6) / 1e9,
+                    "frac_of_step_ceiling": total / (us * 1e-6) / 1e9 / hbm, "peak_kind": kind}
+        del s
+        torch.cuda.empty_cache()
+    return out
+
+
+# ----------------------------------------------------------------------------
+# chained decode rounds as one CUDA graph
+# ----------------------------------------------------------------------------
+def measure_rounds(step, rounds=16, layers=32, iters=20, warmup=3, seed=31):
+    """`rounds` chained decode rounds of the Vicuna-7B-shaped batch-1 workload
+    captured as one CUDA graph: round r + 1's root token is round r's next
+    token, its heads read round r's h_next, and its KV prefix is round r's
+    compacted cache (kv_len grows by accept_len + 1 per round).  Per round:
+    heads -> build_tree -> the round's tree K/V rows written into every
+    layer's cache at slots [kv_len, kv_len + N) (the backbone's part, from a
+    pool drawn ahead) -> tree attention over `layers` layers -> verifier logits
+    planted around the round's own candidates (the lowest-index child of a node
+    carries its row's argmax with probability 0.8, drawn ahead) -> greedy
+    acceptance -> one compaction of every layer's cache.  Reports graph time per
+    round, rounds/s and accepted tokens per wall-second (sum of accept_len + 1
+    over the rounds, read after the timed replays)."""
+    import torch
+    M, c = step.M, CFG
+    dev = step.h.device
+    B, N, Dmax, Hkv, D, H, V = c["B"], step.N, step.Dmax, c["Hkv"], c["D"], c["H"], c["V"]
+    if B != 1:
+        return None
+    L0 = int(step.kv_len0[0].item())
+    Lmax = L0 + N + rounds * (Dmax + 1)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    bf = torch.bfloat16
+    kc = torch.randn(B, layers * Hkv, Lmax, D, device=dev, generator=g).to(bf)
+    vc = torch.randn(B, layers * Hkv, Lmax, D, device=dev, generator=g).to(bf)
+    kls = [kc[:, l * Hkv:(l + 1) * Hkv] for l in range(layers)]
+    vls = [vc[:, l * Hkv:(l + 1) * Hkv] for l in range(layers)]
+    tk = torch.randn(rounds, B, layers * Hkv, N, D, device=dev, generator=g).to(bf)  # tree K/V rows per round
+    tv = torch.randn(rounds, B, layers * Hkv, N, D, device=dev, generator=g).to(bf)
+    qs = torch.randn(rounds, B, N, c["Hq"], D, device=dev, generator=g).to(bf)
+    hts = torch.randn(rounds, B, N, H, device=dev, generator=g).to(bf)
+    base = torch.randn(B, N, V, device=dev, generator=g)  # N(0, 1) verifier rows
+    parent = step.t["parent"]
+    first_child = np.zeros(N, np.int64)
+    has_child = np.zeros(N, bool)
+    for j in range(N - 1, 0, -1):
+        first_child[parent[j]] = j
+        has_child[parent[j]] = True
+    fc = torch.from_numpy(first_child).to(dev)
+    plant = (torch.rand(rounds, B, N, device=dev, generator=g) < c["alpha"]) & torch.from_numpy(has_child).to(dev)
+    plant_val = plant.float() * 100.0  # far above any N(0, 1) draw
+    vwork = torch.empty_like(base)
+    ar = torch.arange(N, device=dev)
+    h0, root0 = step.h.clone(), step.root.clone()
+    h_cur, root_cur = torch.empty_like(h0), torch.empty_like(root0)
+    kv_len = torch.empty_like(step.kv_len0)
+    tokens = torch.zeros(1, dtype=torch.int64, device=dev)
+    i32 = torch.int32
+    idx = torch.empty(B, c["K"], c["topk"], dtype=i32, device=dev)
+    val = torch.empty(B, c["K"], c["topk"], device=dev)
+    cand = torch.empty(B, N, dtype=i32, device=dev)
+    att_out = torch.empty(B, N, c["Hq"], D, device=dev)
+    acc = dict(accept_len=torch.empty(B, dtype=i32, device=dev), best_node=torch.empty(B, dtype=i32, device=dev),
+               path_nodes=torch.empty(B, Dmax + 1, dtype=i32, device=dev), next_tok=torch.empty(B, dtype=i32, device=dev))
+    h_next = torch.empty_like(h0)
+    src = torch.empty(B, Dmax + 1, dtype=i32, device=dev)
+    ws_att = torch.empty(max(16, M.tree_attention_workspace(B, N, c["Hq"], Hkv, D, Lmax)), dtype=torch.uint8,
+                         device=dev)
+
+    def one():
+        kv_len.copy_(step.kv_len0)
+        h_cur.copy_(h0)
+        root_cur.copy_(root0)
+        tokens.zero_()
+        for r in range(rounds):
+            M.heads_topk(h_cur, step.w1, step.b1, step.w2, c["topk"], out=(idx, val, None), ws=step.ws_heads)
+            M.build_tree(idx, root_cur, step.depth, step.rank, out=cand)
+            slots = kv_len[0].long() + ar  # batch 1: one set of slots
+            kc.index_copy_(2, slots, tk[r])
+            vc.index_copy_(2, slots, tv[r])
+            for l in range(layers):
+                M.tree_attention(qs[r], kls[l], vls[l], kv_len, step.mask, step.scale, out=att_out, ws=ws_att)
+            vwork.copy_(base)
+            vwork.view(B * N, V).scatter_add_(1, cand[:, fc].reshape(B * N, 1).long(),
+                                              plant_val[r].reshape(B * N, 1))
+            M.verify_accept_tree(vwork, cand, step.parent, step.depth, Dmax, out=acc, ws=step.ws_ver)
+            M.kv_compact(kc, vc, kv_len, acc["path_nodes"], acc["accept_len"], acc["best_node"], N, Dmax,
+                         hidden_tree=hts[r], h_next=h_next, src_idx=src)
+            tokens.add_(acc["accept_len"].sum() + B)
+            h_cur.copy_(h_next)
+            root_cur.copy_(acc["next_tok"])
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            one()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        one()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    us_round = a.elapsed_time(b) * 1e3 / (iters * rounds)
+    tok = int(tokens.item())  # of the last replay (every replay starts from the same state)
+    grown = int(kv_len[0].item()) - L0
+    out = {"rounds": rounds, "layers": layers, "us_per_round": us_round, "rounds_per_s": 1e6 / us_round,
+           "tokens_per_round": tok / rounds, "tokens_per_s": tok / rounds * 1e6 / us_round,
+           "kv_len_growth": grown, "graph_replays": iters}
+    del kc, vc, tk, tv, qs, hts
+    torch.cuda.empty_cache()
+    return out
+
+
+# ----------------------------------------------------------------------------
+# speculative-sampling acceptance sweep
+# ----------------------------------------------------------------------------
+def expected_tokens(alpha, gamma):
+    """Expected tokens per round, (1 - alpha^(gamma+1)) / (1 - alpha), gamma + 1
+    at alpha = 1 (speculative-decoding e-book page, "Expected tokens per round")."""
+    if alpha >= 1.0:
+        return gamma + 1.0
+    return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)
+
+
+def measure_chain_sweep(dev, rounds=64, sigmas=(0.1, 0.5, 1.0), gmax=32, B=64, V=128256):
+    """medusa_verify_accept_chain over sigma x gamma = 0..gmax, `rounds` rounds
+    each, batch 64, vocab 128256.  Every round draws, on the GPU and untimed,
+    ql ~ N(0, 2) for gmax + 1 positions, q = softmax(ql), p = softmax(ql +
+    N(0, sigma)) and drafts x_i ~ q_i; the call at gamma reads the first gamma
+    + 1 rows of p and gamma rows of q (copied into buffers of their own, then L2
+    flushed by a 256 MB write, so each timed call reads HBM).  Reported per
+    (sigma, gamma): measured alpha = accepted / drafts examined, alpha =
+    mean over positions of sum_v min(p, q) (1 - total variation), mean tokens
+    per round next to E(alpha_hat, gamma) and E(alpha, gamma), the median call
+    time, rounds/s and tokens/s; plus the HBM roofline of the call at
+    gamma = 1, 4, 8, 32 (sigma 0.5)."""
     import torch
     import medusa_speculative_decoding_gb300 as M
-    B, V = 64, 128256
-    hbm, _ = _peaks()
+    hbm, kind = _peaks()
     g = torch.Generator(device=dev)
-    g.manual_seed(5)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    out = {}
-    for gamma in gammas:
-        ql = torch.randn(B, gamma + 1, V, device=dev, generator=g) * 2.0
-        p = torch.softmax(ql + sigma * torch.randn(B, gamma + 1, V, device=dev, generator=g), -1)
-        q = torch.softmax(ql[:, :gamma], -1).contiguous()
-        draft = torch.multinomial(q.reshape(-1, V), 1, generator=g).reshape(B, gamma).to(torch.int32)
-        del ql
-        ws = torch.empty(max(16, M.verify_chain_workspace(B, gamma, V)), dtype=torch.uint8, device=dev)
-        n_acc = torch.empty(B, dtype=torch.int32, device=dev)
-        toks = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
-        ts, by = [], []
-        for r in range(reps + 2):
-            flush.fill_(r & 255)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            M.verify_accept_chain(p, q, draft, 1234, r, out=(n_acc, toks), ws=ws)
-            b.record()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(16, M.verify_chain_workspace(B, gmax, V)), dtype=torch.uint8, device=dev)
+    n_acc = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty(B, gmax + 1, dtype=torch.int32, device=dev)
+    res = {}
+    roof = {}
+    for si, sigma in enumerate(sigmas):
+        acc = torch.zeros(gmax + 1, dtype=torch.float64, device=dev)
+        exam = torch.zeros_like(acc)
+        tok = torch.zeros_like(acc)
+        by = torch.zeros_like(acc)
+        asum = torch.zeros_like(acc)
+        times = [[] for _ in range(gmax + 1)]
+        for r in range(rounds):
+            g.manual_seed(5_000_000 + 1000 * si + r)
+            ql = torch.randn(B, gmax + 1, V, device=dev, generator=g) * 2.0
+            p = torch.softmax(ql + sigma * torch.randn(B, gmax + 1, V, device=dev, generator=g), -1)
+            q = torch.softmax(ql[:, :gmax], -1)
+            del ql
+            draft = torch.multinomial(q.reshape(-1, V), 1, generator=g).reshape(B, gmax).to(torch.int32)
+            amin = torch.minimum(p[:, :gmax], q).sum(-1, dtype=torch.float64)  # [B, gmax]
+            evs = []
+            for gam in range(gmax + 1):
+                P = p[:, :gam + 1].contiguous()
+                Q = q[:, :gam].contiguous() if gam else None
+                Dr = draft[:, :gam].contiguous() if gam else None
+                flush.fill_(r & 255)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                M.verify_accept_chain(P, Q, Dr, 1234 + si, r, out=(n_acc, toks), ws=ws)
+                e1.record()
+                evs.append((e0, e1))
+                n = n_acc.to(torch.float64)
+                acc[gam] += n.sum()
+                if gam:
+                    exam[gam] += torch.minimum(n + 1, torch.full_like(n, gam)).sum()
+                    asum[gam] += amin[:, :gam].mean(1).sum()
+                tok[gam] += (n + 1).sum()
+                by[gam] += (8 * torch.minimum(n + 1, torch.full_like(n, gam))
+                            + torch.where(n == gam, 4.0 * V, 8.0 * V)).sum()
+                del P, Q, Dr
             torch.cuda.synchronize()
-            if r >= 2:
-                ts.append(a.elapsed_time(b) * 1e3)
-                na = n_acc.cpu().numpy()
-                by.append(int(sum((8 * (int(n) + 1) + (4 * V if n == gamma else 8 * V)) for n in na)))
-        us = statistics.median(ts)
-        bb = statistics.mean(by)
-        out[f"gamma{gamma}"] = {"us": us, "algorithmic_bytes": bb, "gbs": bb / (us * 1e-6) / 1e9,
-                                "frac_hbm": bb / (us * 1e-6) / 1e9 / hbm}
-        del p, q, draft, ws
-    del flush
-    return out
+            for gam, (e0, e1) in enumerate(evs):
+                times[gam].append(e0.elapsed_time(e1) * 1e3)
+            del p, q, draft, amin
+        acc, exam, tok, by, asum = (x.cpu().numpy() for x in (acc, exam, tok, by, asum))
+        rows = {}
+        for gam in range(gmax + 1):
+            us = statistics.median(times[gam])
+            a_hat = float(acc[gam] / exam[gam]) if gam else None
+            a_th = float(asum[gam] / (rounds * B)) if gam else None
+            mean_tok = float(tok[gam] / (rounds * B))
+            rows[str(gam)] = {
+                "alpha_hat": None if a_hat is None else round(a_hat, 5),
+                "alpha": None if a_th is None else round(a_th, 5),
+                "tokens_per_round": round(mean_tok, 5),
+                "E_alpha_hat": round(expected_tokens(a_hat, gam), 5) if gam else 1.0,
+                "E_alpha": round(expected_tokens(a_th, gam), 5) if gam else 1.0,
+                "us": round(us, 2), "rounds_per_s": round(1e6 / us, 1),
+                "tokens_per_s": round(mean_tok * B * 1e6 / us, 1)}
+            if sigma == 0.5 and gam in (1, 4, 8, 32):
+                bb = float(by[gam] / rounds)
+                roof[f"gamma{gam}"] = {"us": us, "algorithmic_bytes": bb, "gbs": bb / (us * 1e-6) / 1e9,
+                                       "frac_hbm": bb / (us * 1e-6) / 1e9 / hbm, "peak_kind": kind}
+        res[f"sigma{sigma}"] = rows
+    del flush, ws
+    torch.cuda.empty_cache()
+    return {"rounds": rounds, "batch": B, "vocab": V, "sweep": res}, roof
 
 
 # ----------------------------------------------------------------------------
 # oracle timing (CPU baseline and the reference arm)
 # ----------------------------------------------------------------------------
-class OracleSample:
-    """Times the CPU oracle on a bounded sample of the step and scales each
-    component to the full step: heads of one head restricted to nv vocab rows
-    (its W1 in full), R attention query rows, the full verify and compaction."""
+def host_cores():
+    """Threads this process may run on (its CPU affinity mask)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
-    def __init__(self, inp, nv, R):
+
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (model name on x86; implementer
+    and part numbers on Arm, e.g. 0x41/0xd4f for Neoverse V2)."""
+    import platform
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model"):
+        for ln in info.splitlines():
+            if ln.startswith(key):
+                return ln.split(":", 1)[1].strip()
+    imp = [ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU implementer")]
+    part = [ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU part")]
+    return f"{platform.machine()} implementer {imp[0] if imp else '?'} part {part[0] if part else '?'}"
+
+
+class OracleStep:
+    """The whole decode step in the oracle (float64 C): every head and vocab
+    row, the top-k and candidates, every attention row, greedy acceptance of
+    the planted verifier logits, compaction.  Steps share only read-only
+    inputs, so independent steps run concurrently on host threads (the C
+    oracle releases the interpreter lock)."""
+
+    def __init__(self, inp):
         from oracle import oracle as O
-        self.O = O
-        self.inp = inp
-        self.nv, self.R = nv, R
-        c = CFG
+        self.O, self.inp, c = O, inp, CFG
         self.t = t = O.tree_layout(O.sparse_tree_paths(64, 5, 8, 0.6, 0.5), 5)
-        self.N = t["N"]
-        rng = np.random.default_rng(0)
-        self.rows = np.stack([np.zeros(R, int), rng.integers(0, self.N, R), rng.integers(0, c["Hq"], R)],
-                             1).astype(np.int32)
-        self.cand = O.build_tree(W.random_topk_lists(2, c["B"], c["K"], c["topk"], c["V"]), inp["root"],
-                                 t["depth"], t["rank"])
-        self.vlogits = W.planted_logits(CFG["seed"], self.cand, t["parent"], c["V"], c["alpha"])
-        self.hd = inp["heads"]
+        hd = inp["heads"]
+        lg = O.heads_logits(hd["h"], hd["w1"], hd["b1"], hd["w2"], c["dtype"])
+        idx, _ = O.topk(lg, c["topk"])
+        cand = O.build_tree(idx, inp["root"], t["depth"], t["rank"])
+        self.vlogits = W.planted_logits(c["seed"], cand, t["parent"], c["V"], c["alpha"])
 
-    def step(self, k):
-        """One sample step; returns the scaled full-step seconds."""
-        O, c, t = self.O, CFG, self.t
-        K, H, V, nv = c["K"], c["H"], c["V"], self.nv
-        hd = self.hd
-        k = k % K
+    def step(self, _=None):
+        O, c, t, inp = self.O, CFG, self.t, self.inp
+        hd = inp["heads"]
         t0 = time.perf_counter()
-        O.heads_logits(hd["h"], hd["w1"][k:k + 1], hd["b1"][k:k + 1], hd["w2"][k:k + 1, :nv], c["dtype"])
-        t1 = time.perf_counter()
-        O.tree_attention(self.inp["att"]["q"], self.inp["att"]["k_cache"], self.inp["att"]["v_cache"],
-                         self.inp["kv_len"], t["mask"], c["dtype"], 1 / np.sqrt(c["D"]), rows=self.rows)
-        t2 = time.perf_counter()
-        r = O.verify_tree(self.vlogits, self.cand, t["parent"], t["depth"], t["max_depth"])
-        t3 = time.perf_counter()
-        O.kv_compact(self.inp["att"]["k_cache"], self.inp["att"]["v_cache"], self.inp["kv_len"],
-                     r["path_nodes"], r["accept_len"], r["best_node"], self.inp["ht"], self.N, t["max_depth"])
-        t4 = time.perf_counter()
-        heads_scale = K * (H * H + V * H) / (H * H + nv * H)
-        att_scale = c["B"] * self.N * c["Hq"] / self.R
-        return (t1 - t0) * heads_scale + (t2 - t1) * att_scale + (t3 - t2) + (t4 - t3)
+        lg = O.heads_logits(hd["h"], hd["w1"], hd["b1"], hd["w2"], c["dtype"])
+        idx, _ = O.topk(lg, c["topk"])
+        cand = O.build_tree(idx, inp["root"], t["depth"], t["rank"])
+        O.tree_attention(inp["att"]["q"], inp["att"]["k_cache"], inp["att"]["v_cache"], inp["kv_len"], t["mask"],
+                         c["dtype"], 1 / np.sqrt(c["D"]))
+        r = O.verify_tree(self.vlogits, cand, t["parent"], t["depth"], t["max_depth"])
+        O.kv_compact(inp["att"]["k_cache"], inp["att"]["v_cache"], inp["kv_len"], r["path_nodes"], r["accept_len"],
+                     r["best_node"], inp["ht"], t["N"], t["max_depth"])
+        return time.perf_counter() - t0
 
 
-def oracle_cores():
-    return 1  # the oracle is single-threaded C
+def oracle_throughput(inp, steps, warmup):
+    """Runs `warmup` then `steps` full oracle steps, spread over every host core
+    (one step per thread at a time); returns (steps/s of the timed steps, wall
+    seconds, mean seconds of one step, threads)."""
+    import concurrent.futures as cf
+    s = OracleStep(inp)
+    n = host_cores()
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        if warmup:
+            list(ex.map(s.step, range(warmup)))
+        t0 = time.perf_counter()
+        per = list(ex.map(s.step, range(steps)))
+        wall = time.perf_counter() - t0
+    return steps / wall, wall, statistics.mean(per), min(n, steps)
 
 
 def cpu_baseline(inp):
-    s = OracleSample(inp, nv=CFG["V"], R=256)
-    secs = [s.step(k) for k in range(2)]
-    est = statistics.mean(secs)
-    return {"value": 1.0 / est, "unit": "steps/s", "cores": oracle_cores(), "kind": "oracle",
-            "sample": "2 sample steps: one head in full (W1 and all 32000 W2 rows), 256 of 2048 "
-                      "attention query rows, full greedy verify and compaction; each component "
-                      "scaled to the full step; single-threaded float64 C"}
+    """The oracle on the host: one full step per host thread, all at once
+    (about one step's time of wall clock)."""
+    n = host_cores()
+    val, wall, per, used = oracle_throughput(inp, steps=n, warmup=0)
+    return {"value": val, "unit": "steps/s", "cores": used, "kind": "oracle", "cpu_model": cpu_model(),
+            "single_step_s": per,
+            "sample": f"{n} full oracle steps of the workload (every head and vocab row, every attention row, "
+                      f"full verify and compaction; float64 C), one per host thread, run together in "
+                      f"{wall:.1f} s"}
 
 
 # ----------------------------------------------------------------------------
@@ -829,24 +1172,19 @@ def main():
         if rank != 0:
             return 0
         inp = make_inputs_host_only()
-        budget = 150.0 / (args.steps + args.warmup)
-        nv, R = (1024, 16) if budget > 0.08 else (128, 4)
-        s = OracleSample(inp, nv=nv, R=R)
-        for k in range(args.warmup):
-            s.step(k)
-        t0 = time.perf_counter()
-        est = [s.step(k) for k in range(args.steps)]
-        wall = time.perf_counter() - t0
-        T = statistics.mean(est)
-        val = 1.0 / T
+        val, wall, per, used = oracle_throughput(inp, args.steps, args.warmup)
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "steps/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": T * 1e3,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": {"workload": WORKLOAD, "sample_wall_s": wall},
-                "cpu_baseline": {"value": val, "unit": "steps/s", "cores": oracle_cores(), "kind": "oracle",
-                                 "sample": f"per step: one head with {nv} of 32000 W2 rows (W1 in full), "
-                                           f"{R} of 2048 attention query rows, full verify and "
-                                           "compaction; each component scaled to the full step"},
+                "data": "synthetic",
+                "config": {"workload": WORKLOAD, "timed_wall_s": wall, "single_step_s": per,
+                           "extrapolated": False},
+                "cpu_baseline": {"value": val, "unit": "steps/s", "cores": used, "kind": "oracle",
+                                 "cpu_model": cpu_model(),
+                                 "sample": f"{args.steps} full oracle steps (every head and vocab row, every "
+                                           f"attention row, full verify and compaction; float64 C) after "
+                                           f"{args.warmup} warm-up steps, spread over {used} host threads, "
+                                           f"one step per thread at a time"},
                 "e2e": {"value": val, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return 0
@@ -911,12 +1249,15 @@ def main():
     e2e_s, h2d, d2h = run_e2e(step, max(20, K // 4), args.warmup)
     e2e_val = world * max(20, K // 4) / e2e_s
 
-    graph = measure_step_graph(step) if world == 1 or rank == 0 else None
-    trees = measure_tree_sizes(step) if world == 1 or rank == 0 else None
-    proj = measure_projection(dev) if world == 1 or rank == 0 else None
-    att_w = measure_attention_workloads(dev) if world == 1 or rank == 0 else None
-    chain = measure_chain(dev) if world == 1 or rank == 0 else None
-    heads_b = measure_heads_batches(dev) if world == 1 or rank == 0 else None
+    lead = world == 1 or rank == 0
+    graph = measure_step_graph(step) if lead else None
+    rounds = {"layers1": measure_rounds(step, layers=1), "layers32": measure_rounds(step, layers=32)} if lead else None
+    trees = measure_tree_sizes(step) if lead else None
+    steps_w = measure_workload_steps(dev) if lead else None
+    proj = measure_projection(dev) if lead else None
+    att_w = measure_attention_workloads(dev) if lead else None
+    sweep, chain = measure_chain_sweep(dev) if lead else (None, None)
+    heads_b = measure_heads_batches(dev) if lead else None
 
     peak, peak_kind = _peaks()
     hb, ab, vb = algorithmic_bytes(c, N, int(inp["kv_len"][0]) + N)
@@ -941,10 +1282,13 @@ def main():
             "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
             "step_ms_distribution": step_dist,
             "step_graph_32_layers": graph,
+            "chained_rounds": rounds,
             "tree_sizes": trees,
+            "workload_steps": steps_w,
             "verify_projection": proj,
             "attention_workloads": att_w,
             "chain_acceptance": chain,
+            "chain_sweep": sweep,
             "heads_batches": heads_b,
             "clocks": clocks,
             "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d,

@@ -44,3 +44,18 @@ def test_workloads_have_distinct_seeds():
     seeds = [w["seed"] for w in W.WORKLOADS.values()]
     assert len(seeds) == len(set(seeds)) == 5
     assert np.all(np.array(seeds) > 0)
+
+
+def test_expected_tokens_of_the_sweep_report():
+    # the sweep's E(alpha, gamma) is the cost model's closed form (the oracle's
+    # analytic module, pinned to the page's printed numbers)
+    from oracle import analytic as A
+    for a in (0.0, 0.3, 0.8, 0.99, 1.0):
+        for g in (0, 1, 4, 32):
+            assert abs(bench.expected_tokens(a, g) - A.expected_tokens(a, g)) < 1e-12
+    assert abs(bench.expected_tokens(0.8, 4) - 3.3616) < 1e-12
+
+
+def test_host_description():
+    assert bench.host_cores() >= 1
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
