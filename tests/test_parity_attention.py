@@ -47,6 +47,13 @@ def _run(M, x, kv_len, t, scale):
     ("root", 2, 4, 4, 128, [0, 100], 110, "bf16"),
     ("root", 1, 8, 2, 64, [300], 310, "bf16"),
     ("max512", 1, 4, 2, 64, [129], 650, "f32"),
+    # batch 1 with <= 64 query rows per block (rows spread over the four TMEM
+    # lane quarters, split partials merged through the receive area), D 128
+    # and 64, GQA, empty and long prefixes
+    ("sparse64", 1, 4, 4, 128, [0], 80, "bf16"),
+    ("c1", 1, 8, 2, 128, [500], 520, "bf16"),
+    ("sparse64", 1, 2, 2, 64, [1000], 1100, "bf16"),
+    ("small", 1, 6, 2, 128, [4000], 4100, "bf16"),
 ])
 def test_attention_full_compare(medusa, kind, B, Hq, Hkv, D, lens, Lmax, dtype):
     t = _tree(kind)
