@@ -1158,6 +1158,8 @@ def main():
                          "5 heads, top-8, bf16, random-init weights) --steps times, print the last "
                          "call's time, and exit")
     ap.add_argument("--hidden", type=int, default=4096)
+    ap.add_argument("--only-step", action="store_true",
+                    help="profiling aid: run --warmup then --steps headline steps, print their time, and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1209,6 +1211,15 @@ def main():
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
+    if args.only_step:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            step.run()
+        b.record()
+        torch.cuda.synchronize()
+        print(json.dumps({"only_step": True, "steps": args.steps, "us_per_step": a.elapsed_time(b) * 1e3 / args.steps}))
+        return 0
 
     K = args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

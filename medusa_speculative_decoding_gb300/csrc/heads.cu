@@ -384,12 +384,15 @@ int launch_heads(const void* h, const void* w1, const void* b1, const void* w2, 
         cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem1);
     if (p.smem2 > 48 * 1024)
         cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem2);
-    // K1 grid: exactly the CTAs that fit on the device at once, but no more
-    // warps than row groups.
+    // K1 grid: one wave of at most two CTAs per SM (no more warps than row
+    // groups).  The rest of each SM stays free for K2's CTAs, which launch as
+    // programmatic dependents while K1 runs: they load their set-up and warm L2
+    // with their first W2 rows before K1 ends (batch-1 step: 268 -> 265 us
+    // against a full K1 wave of four CTAs per SM).
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k1, THREADS, p.smem1) != cudaSuccess || occ < 1)
         occ = 1;
-    long long grid1 = (long long)sm_count() * occ;
+    long long grid1 = (long long)sm_count() * (occ < 2 ? occ : 2);
     const long long groups = (long long)K * H / kRows1;
     const long long max_ctas = (groups + THREADS / 32 - 1) / (THREADS / 32);
     if (grid1 > max_ctas) grid1 = max_ctas;

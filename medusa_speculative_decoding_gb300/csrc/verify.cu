@@ -287,15 +287,19 @@ __global__ void __launch_bounds__(kChainThreads) chain_scan_kernel(
     const int v0 = c * kChainChunk, v1 = min(V, v0 + kChainChunk);
     // The thread's best race key is kept as the fraction be / bw (E = -ln U+,
     // w the weight) and compared by cross-multiplication (one division per
-    // thread, not per element).  The largest p is tracked without its index:
-    // the index is looked up afterwards, only when no weight is positive.
+    // thread, not per element).  On the 16-byte path the largest p is not
+    // tracked: it is found by a second read of the chunk, only when no weight
+    // of the chunk is positive (the scalar path tracks it, without its index).
     //
     // Pruning: once the CTA has seen keys, kb bounds its best key from above.
     // Since -ln U >= 1 - U, an element with (1 - U) > kb * w * (1 + 2^-10) has a
     // key more than 2^-11 (relative) above a key already seen: it can neither
     // win nor tie, so its logarithm and comparison are skipped (by the whole
     // warp when no lane needs them).  The margin is far above the float32
-    // rounding of logf, the products and kb itself.
+    // rounding of logf, the products and kb itself.  On the 16-byte path the
+    // test reads 2^24 (1 - U) = 2^24 - 1 - bits exactly as an integer, a warp
+    // votes once per group of four entries, and every lane runs every group
+    // (groups past the chunk are zeros and need nothing).
     float be = INFINITY, bw = 1.f, pm = -INFINITY;
     int bt = INT_MAX;
     float kb = INFINITY;
@@ -341,23 +345,40 @@ __global__ void __launch_bounds__(kChainThreads) chain_scan_kernel(
         // v/2 + 2; the generator state is advanced by additions
         const uint64_t zstep = (uint64_t)(2 * kChainThreads) * kSmGamma;
         uint64_t z = key + (uint64_t)((v0 >> 1) + 2 * threadIdx.x + 1) * kSmGamma;
+        float thr = INFINITY;  // 2^24 kb (1 + 2^-10)
 #pragma unroll
         for (int k = 0; k < kPer; ++k, z += zstep) {
             const int v = v0 + 4 * (threadIdx.x + kChainThreads * k);
             const bool in = v < v1;
-            uint64_t h0 = 0;
-            if (in) {
-                h0 = sm_mix(z);
-                take(__uint_as_float(pw[k].x), __uint_as_float(qw[k].x), v, race_u_even(h0));
+            const uint64_t h0 = sm_mix(z), h1 = sm_mix(z + kSmGamma);
+            const uint32_t bits[4] = {(uint32_t)(h0 >> 40), (uint32_t)(h0 >> 16) & 0xFFFFFFu,
+                                      (uint32_t)(h1 >> 40), (uint32_t)(h1 >> 16) & 0xFFFFFFu};
+            const float pv[4] = {__uint_as_float(pw[k].x), __uint_as_float(pw[k].y), __uint_as_float(pw[k].z),
+                                 __uint_as_float(pw[k].w)};
+            const float qv[4] = {__uint_as_float(qw[k].x), __uint_as_float(qw[k].y), __uint_as_float(qw[k].z),
+                                 __uint_as_float(qw[k].w)};
+            float w[4];
+            bool need[4], any = false;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                w[i] = bonus ? pv[i] : pv[i] - qv[i];
+                need[i] = in && w[i] > 0.f && !((float)(0xFFFFFFu - bits[i]) > thr * w[i]);
+                any |= need[i];
             }
-            if (k == 0) refresh_bound();  // after one element per thread
-            if (in) {
-                take(__uint_as_float(pw[k].y), __uint_as_float(qw[k].y), v + 1, race_u_odd(h0));
-                const uint64_t h1 = sm_mix(z + kSmGamma);
-                take(__uint_as_float(pw[k].z), __uint_as_float(qw[k].z), v + 2, race_u_even(h1));
-                take(__uint_as_float(pw[k].w), __uint_as_float(qw[k].w), v + 3, race_u_odd(h1));
+            if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (need[i]) {
+                        const float e = -logf((float)(bits[i] + 1u) * (1.0f / 16777216.0f));
+                        const float lhs = e * bw, rhs = be * w[i];
+                        if (lhs < rhs || (lhs == rhs && v + i < bt)) { be = e; bw = w[i]; bt = v + i; }
+                    }
+                }
             }
-            if (k == 0) refresh_bound();  // after the first group of four
+            if (k == 0) {
+                refresh_bound();
+                thr = kb * (16777216.f * (1.f + 1.f / 1024.f));
+            }
         }
     } else {
         for (int v = v0 + threadIdx.x; v < v1; v += kChainThreads)
@@ -374,6 +395,8 @@ __global__ void __launch_bounds__(kChainThreads) chain_scan_kernel(
     __shared__ ChainPart sp[kChainThreads / 32];
     __shared__ ChainPart s_r;
     __shared__ int s_pidx;
+    __shared__ float s_pm;
+    if (threadIdx.x == 0) s_pm = -INFINITY;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) sp[warp] = ChainPart{bk, bt, pm, INT_MAX};
     if (threadIdx.x == 0) s_pidx = INT_MAX;
@@ -389,6 +412,16 @@ __global__ void __launch_bounds__(kChainThreads) chain_scan_kernel(
     }
     __syncthreads();
     ChainPart r = s_r;
+    if (r.tok == INT_MAX && vec) {
+        // (lean path) the chunk's largest p was not tracked: find it now
+        float m2 = -INFINITY;
+        for (int v = v0 + threadIdx.x; v < v1; v += kChainThreads) m2 = fmaxf(m2, pr[v]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+        if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<int*>(&s_pm), __float_as_int(m2));
+        __syncthreads();
+        r.pmax = s_pm;
+    }
     if (r.tok == INT_MAX) {
         // no positive weight in this chunk: the lowest token holding its largest
         // p, for the fallback (rare; the chunk is read again)

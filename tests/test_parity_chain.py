@@ -48,6 +48,38 @@ def test_chain_small(medusa, B, gamma, V, sigma):
         assert ((out >= 0).sum(1) == n_acc + 1).all()  # k + 1 tokens
 
 
+@pytest.mark.parametrize("B,gamma,V,sigma", [
+    # scalar path (vocab not a multiple of 4: rows not 16-byte aligned)
+    (5, 3, 999, 0.5), (3, 0, 1001, 0.1),
+    # 16-byte path at its edges: rows shorter than a warp's first group, a
+    # single chunk per sequence, a ragged last chunk, chunks ending inside a
+    # warp's groups
+    (1, 2, 8, 0.5), (3, 1, 4, 1.0), (2, 5, 2044, 0.5), (7, 2, 2052, 0.5), (64, 1, 2048, 0.3),
+    (4, 3, 8196, 0.5)])
+def test_chain_paths_and_edges(medusa, B, gamma, V, sigma):
+    x = W.chain_inputs(seed=B * 13 + gamma, B=B, gamma=gamma, V=V, sigma=sigma)
+    for rnd in range(3):
+        n_acc, out = _gpu(medusa, x, 4321, rnd)
+        ref = O.verify_chain(x["p"], x["q"], x["draft"], 4321, rnd)
+        assert _compare(n_acc, out, ref) <= 1
+        assert ((out >= 0).sum(1) == n_acc + 1).all()
+
+
+def test_chain_misaligned_rows_take_the_scalar_path(medusa):
+    # p and q one float past a 16-byte boundary: the same results
+    B, gamma, V = 6, 3, 4096
+    x = W.chain_inputs(seed=17, B=B, gamma=gamma, V=V, sigma=0.5)
+    P = torch.empty(x["p"].size + 1, device="cuda")[1:].view(B, gamma + 1, V)
+    Q = torch.empty(x["q"].size + 1, device="cuda")[1:].view(B, gamma, V)
+    P.copy_(to_dev(x["p"]))
+    Q.copy_(to_dev(x["q"]))
+    for rnd in range(2):
+        n_acc, out = medusa.verify_accept_chain(P, Q, to_dev(x["draft"]), 7, rnd)
+        torch.cuda.synchronize()
+        ref = O.verify_chain(x["p"], x["q"], x["draft"], 7, rnd)
+        assert _compare(to_np(n_acc), to_np(out), ref) <= 1
+
+
 @pytest.mark.parametrize("gamma,sigma", [(0, 0.1), (1, 0.5), (4, 1.0), (8, 0.1), (32, 0.5)])
 def test_chain_full_size(medusa, gamma, sigma):
     c = W.WORKLOADS["chain_b64_v128256"]
