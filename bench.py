@@ -64,7 +64,7 @@ WORKLOAD = ("vicuna7b-shaped medusa step, batch 1: hidden 4096, vocab 32000, 5 h
 # DRAM bytes per launch of the heads call, from the ncu capture summarised in
 # profiles/ (dram__bytes_read.sum + dram__bytes_write.sum summed over its three
 # kernels), with the sha1 of heads.cu it was taken on; null once that file changes.
-HEADS_TRAFFIC = {"sha1": "59db57fcb6ec1b9d1cb3888505e2d04db70349b0", "bytes": 1479522091}
+HEADS_TRAFFIC = {"sha1": "0767f4c9c673445c393a5d345066140df4f30dee", "bytes": 1478950826}
 
 
 def _sha1(path):
@@ -1159,7 +1159,11 @@ def main():
                          "call's time, and exit")
     ap.add_argument("--hidden", type=int, default=4096)
     ap.add_argument("--only-step", action="store_true",
-                    help="profiling aid: run --warmup then --steps headline steps, print their time, and exit")
+                    help="profiling aid: run --warmup then --steps steps of --workload, print their time, and exit")
+    ap.add_argument("--workload", default="h4096_b1_sparse64",
+                    choices=["h4096_b1_sparse64", "h5120_b8_ragged", "h4096_b4_kv8192_sparse64",
+                             "h4096_b4_kv8192_dense341"],
+                    help="with --only-step: the headline batch-1 step or one of the batched steps")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1203,6 +1207,23 @@ def main():
     if world > 1:
         dist.barrier()
 
+    if args.only_step and args.workload != "h4096_b1_sparse64":
+        name, tree = {"h5120_b8_ragged": ("h5120_b8_ragged", "sparse64"),
+                      "h4096_b4_kv8192_sparse64": ("h4096_b4_kv8192", "sparse64"),
+                      "h4096_b4_kv8192_dense341": ("h4096_b4_kv8192", "dense341")}[args.workload]
+        s = WorkloadStep(name, tree, dev)
+        for _ in range(args.warmup):
+            s.run()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            s.run()
+        b.record()
+        torch.cuda.synchronize()
+        print(json.dumps({"only_step": True, "workload": args.workload, "steps": args.steps,
+                          "us_per_step": a.elapsed_time(b) * 1e3 / args.steps}))
+        return 0
     inp = make_inputs()
     step = Step(inp, dev)
     c = CFG
