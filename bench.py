@@ -320,23 +320,26 @@ def _pack(tensors, device, pinned=False):
 
 def run_e2e(step, steps, warmup):
     """Same step through the C ABI with host buffers: per-step inputs copied from
-    pinned host memory, results read back, all inside the timed region.  The
-    contiguous inputs (h, q, verifier logits, tree hidden states) travel as one
-    packed copy and the results as one packed read; the tree's K/V rows are
-    copied into their cache slots.  The whole step (copies and calls) is one
-    CUDA graph replayed and waited for once per step."""
+    pinned host memory, results read back, all inside the timed region.  Every
+    input (h, q, verifier logits, tree hidden states, the tree's K/V rows)
+    travels in one packed host-to-device copy and the results in one packed
+    read; the tree's K/V rows then move from the staging buffer into their
+    cache slots on the device.  The whole step (copies and calls) is one CUDA
+    graph replayed and waited for once per step."""
     torch = step.torch
     L = int(step.kv_len0[0].item())
     N = step.N
     dev = step.h.device
-    # inputs: one device staging buffer the step reads from, and its pinned twin
+    # inputs: one device staging buffer (the step reads h, q, logits and hidden
+    # states from it; the K/V rows are copied on to the cache) and its pinned twin
     names_in = ("h", "q", "vlogits", "ht")
-    dbuf_in, views = _pack([getattr(step, n) for n in names_in], dev)
+    tree_kv = [step.kc[:, :, L:L + N].contiguous(), step.vc[:, :, L:L + N].contiguous()]
+    dbuf_in, views = _pack([getattr(step, n) for n in names_in] + tree_kv, dev)
     for n, v in zip(names_in, views):
         setattr(step, n, v)
-    hbuf_in, _ = _pack([getattr(step, n).cpu() for n in names_in], "cpu", pinned=True)
-    tk = step.kc[:, :, L:L + N].contiguous().cpu().pin_memory()
-    tv = step.vc[:, :, L:L + N].contiguous().cpu().pin_memory()
+    tk, tv = views[4], views[5]
+    hbuf_in, _ = _pack([getattr(step, n).cpu() for n in names_in] + [t.cpu() for t in tree_kv], "cpu",
+                       pinned=True)
     # results: the step writes them into one device buffer, read back in one copy
     names_out = ("accept_len", "best_node", "path_nodes", "next_tok")
     dbuf_out, outs = _pack([step.acc[n] for n in names_out] + [step.h_next], dev)
@@ -344,13 +347,13 @@ def run_e2e(step, steps, warmup):
         step.acc[n] = v
     step.h_next = outs[4]
     hbuf_out = torch.empty(dbuf_out.numel(), dtype=torch.uint8).pin_memory()
-    h2d = hbuf_in.numel() + tk.numel() * tk.element_size() + tv.numel() * tv.element_size()
+    h2d = hbuf_in.numel()
     d2h = hbuf_out.numel()
 
     def enqueue():
         dbuf_in.copy_(hbuf_in, non_blocking=True)
-        step.kc[:, :, L:L + N].copy_(tk, non_blocking=True)
-        step.vc[:, :, L:L + N].copy_(tv, non_blocking=True)
+        step.kc[:, :, L:L + N].copy_(tk)
+        step.vc[:, :, L:L + N].copy_(tv)
         step.run()
         hbuf_out.copy_(dbuf_out, non_blocking=True)
 
