@@ -52,19 +52,58 @@ __global__ void __launch_bounds__(kStatThreads) row_stats_kernel(const float* __
         if (better(l, v, bv, bi)) { bv = l; bi = v; }
         if (TYPICAL) take_msa(m, s, a, l * inv_t);
     };
-    // vectorised body when the row start is 16-byte aligned
+    // vectorised body when the row start is 16-byte aligned: the thread's
+    // share of the chunk (kPer 16-byte words) is loaded at once; for typical
+    // acceptance its softmax state is formed in two passes over registers (the
+    // maximum, then sum e^(x-m) and sum e^(x-m)(x-m) as independent terms)
+    // instead of an online update per entry, which chains every entry on the
+    // previous one
     const bool vec = ((reinterpret_cast<uintptr_t>(x + v0) & 15u) == 0);
     int v = v0;
     if (vec) {
+        constexpr int kPer = kChunk / (4 * kStatThreads);
         const int nv = (v1 - v0) / 4;
         const float4* x4 = reinterpret_cast<const float4*>(x + v0);
-        for (int i = threadIdx.x; i < nv; i += kStatThreads) {
-            const uint4 r = ld_stream16(x4 + i);
-            const int base = v0 + 4 * i;
-            take(__uint_as_float(r.x), base);
-            take(__uint_as_float(r.y), base + 1);
-            take(__uint_as_float(r.z), base + 2);
-            take(__uint_as_float(r.w), base + 3);
+        float e[4 * kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = threadIdx.x + kStatThreads * k;
+            const uint4 r = i < nv ? ld_stream16(x4 + i) : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+            e[4 * k] = __uint_as_float(r.x);
+            e[4 * k + 1] = __uint_as_float(r.y);
+            e[4 * k + 2] = __uint_as_float(r.z);
+            e[4 * k + 3] = __uint_as_float(r.w);
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = threadIdx.x + kStatThreads * k;
+            if (i < nv) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (better(e[4 * k + j], v0 + 4 * i + j, bv, bi)) { bv = e[4 * k + j]; bi = v0 + 4 * i + j; }
+            }
+        }
+        if (TYPICAL) {
+            // entries past the chunk were loaded as -inf: no probability mass
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 4 * kPer; ++j) {
+                e[j] *= inv_t;
+                mx = fmaxf(mx, e[j]);
+            }
+            if (mx > -INFINITY) {
+                float ss = 0.f, sa = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4 * kPer; ++j) {
+                    const float d = e[j] - mx;  // -inf (empty entries) or NaN: weight 0
+                    const float w = d > -INFINITY ? expf(d) : 0.f;
+                    ss += w;
+                    sa = w > 0.f ? fmaf(w, d, sa) : sa;
+                }
+                m = mx;
+                s = ss;
+                a = sa;
+            }
         }
         v = v0 + 4 * nv;
     }
