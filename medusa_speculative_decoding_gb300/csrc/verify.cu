@@ -33,6 +33,13 @@
 namespace medusa {
 namespace {
 
+// 2^x on the special-function unit (approximate, flush-to-zero)
+__device__ __forceinline__ float exp2_sfu(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 constexpr int kChunk = 4096;     // vocab entries per stats CTA
 constexpr int kStatThreads = 256;
 
@@ -84,7 +91,10 @@ __global__ void __launch_bounds__(kStatThreads) row_stats_kernel(const float* __
             }
         }
         if (TYPICAL) {
-            // entries past the chunk were loaded as -inf: no probability mass
+            // x = logit / T and its maximum exactly as the acceptance kernel
+            // forms them; each weight e^(x - max) on the special-function unit
+            // as 2^((x - max) log2 e).  Entries past the chunk were loaded as
+            // -inf: no probability mass.
             float mx = -INFINITY;
 #pragma unroll
             for (int j = 0; j < 4 * kPer; ++j) {
@@ -96,7 +106,7 @@ __global__ void __launch_bounds__(kStatThreads) row_stats_kernel(const float* __
 #pragma unroll
                 for (int j = 0; j < 4 * kPer; ++j) {
                     const float d = e[j] - mx;  // -inf (empty entries) or NaN: weight 0
-                    const float w = d > -INFINITY ? expf(d) : 0.f;
+                    const float w = d > -INFINITY ? exp2_sfu(d * 1.4426950408889634f) : 0.f;
                     ss += w;
                     sa = w > 0.f ? fmaf(w, d, sa) : sa;
                 }
@@ -168,10 +178,21 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_tree_kernel(const Accep
         const RowStat* st = a.stats + ((size_t)b * N + u) * a.nchunk;
         float bv = -INFINITY, m = -INFINITY, s = 0.f, sa = 0.f;
         int bi = INT_MAX;
-        for (int c = 0; c < a.nchunk; ++c) {
-            const RowStat r = st[c];
-            if (better(r.maxv, r.arg, bv, bi)) { bv = r.maxv; bi = r.arg; }
-            if (TYPICAL) merge_msa(m, s, sa, r.m, r.s, r.a);
+        // the chunk records are loaded eight at a time before they are merged,
+        // so their load latencies overlap instead of chaining
+        constexpr int kBatch = 8;
+        for (int c0 = 0; c0 < a.nchunk; c0 += kBatch) {
+            RowStat rs[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k)
+                if (c0 + k < a.nchunk) rs[k] = st[c0 + k];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (c0 + k < a.nchunk) {
+                    if (better(rs[k].maxv, rs[k].arg, bv, bi)) { bv = rs[k].maxv; bi = rs[k].arg; }
+                    if (TYPICAL) merge_msa(m, s, sa, rs[k].m, rs[k].s, rs[k].a);
+                }
+            }
         }
         s_arg[u] = bi;
         if (TYPICAL) {
