@@ -109,7 +109,7 @@ struct WaitControl {
 std::mutex g_wc_mu;
 // function-local statics: registration runs during static initialisation of
 // the other translation units, whose order is unspecified
-WaitControl* wait_controls(int*) {
+WaitControl* wait_controls() {
     static WaitControl tab[8];
     return tab;
 }
@@ -122,14 +122,14 @@ int& wait_control_count() {
 void register_wait_control(int (*read_clear)(int*, cudaStream_t), int (*set_limit)(long long)) {
     std::lock_guard<std::mutex> lk(g_wc_mu);
     int& n = wait_control_count();
-    if (n < 8) wait_controls(nullptr)[n++] = WaitControl{read_clear, set_limit};
+    if (n < 8) wait_controls()[n++] = WaitControl{read_clear, set_limit};
 }
 
 int wait_controls_read_clear(int* gave_up, cudaStream_t st) {
     std::lock_guard<std::mutex> lk(g_wc_mu);
     const int n = wait_control_count();
     for (int i = 0; i < n; ++i) {
-        const int e = wait_controls(nullptr)[i].read_clear(gave_up, st);
+        const int e = wait_controls()[i].read_clear(gave_up, st);
         if (e) return fail(MEDUSA_ERR_CUDA, "device status: %s", cudaGetErrorString((cudaError_t)e));
     }
     return MEDUSA_OK;
@@ -139,7 +139,7 @@ int wait_controls_set_limit(long long cycles) {
     std::lock_guard<std::mutex> lk(g_wc_mu);
     const int n = wait_control_count();
     for (int i = 0; i < n; ++i) {
-        const int e = wait_controls(nullptr)[i].set_limit(cycles);
+        const int e = wait_controls()[i].set_limit(cycles);
         if (e) return fail(MEDUSA_ERR_CUDA, "set_wait_limit: %s", cudaGetErrorString((cudaError_t)e));
     }
     return MEDUSA_OK;
