@@ -47,6 +47,25 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return r;
 }
 
+
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// (a0, a1) * b + c on the paired float32 pipe
+__device__ __forceinline__ void fma_pair(float a0, float a1, float b, float c, float& d0, float& d1) {
+    asm("{\n.reg .b64 ra, rb, rc, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %4};\nmov.b64 rc, {%5, %5};\n"
+        "fma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (s0, s1) += the two bf16 halves of w (low, high), exactly
+__device__ __forceinline__ void add_bf16_pair(float& s0, float& s1, uint32_t w) {
+    asm("{\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %2;\nadd.rn.f32.bf16 %0, lo, %0;\nadd.rn.f32.bf16 %1, hi, %1;\n}"
+        : "+f"(s0), "+f"(s1) : "r"(w));
+}
+
 struct AttnArgs {
     const uint16_t* q;
     const uint16_t* k;
@@ -398,8 +417,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
                 tmem_wait_ld();
                 const int c0 = kt + q * SW;  // key of sv[0]
                 if (kt == klo && kt + kBlockN <= min(k_end, Lb)) {  // plain prefix tile
+                    float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < SW; ++i) mt = fmaxf(mt, sv[i]);
+                    for (int i = 0; i < SW; i += 4) {
+                        m0 = fmax3(m0, sv[i], sv[i + 1]);
+                        m1 = fmax3(m1, sv[i + 2], sv[i + 3]);
+                    }
+                    mt = fmaxf(m0, m1);
                 } else {
                     uint64_t w0 = 0, w1 = 0;
                     int mbase = 0;
@@ -468,16 +492,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
                 // j & 1: every owner has read its scores before the barrier above
                 const float mr = m_ref == -INFINITY ? 0.f : m_ref;
                 uint32_t pk[SW / 2];
-                float psum = 0.f;
+                float s0 = 0.f, s1 = 0.f;
 #pragma unroll
                 for (int e = 0; e < SW / 2; ++e) {
-                    const float p0 = exp2_approx(fmaf(sv[2 * e], a.scale_log2, -mr));
-                    const float p1 = exp2_approx(fmaf(sv[2 * e + 1], a.scale_log2, -mr));
-                    pk[e] = pack_bf16(p0, p1);
+                    float t0, t1;
+                    fma_pair(sv[2 * e], sv[2 * e + 1], a.scale_log2, -mr, t0, t1);
+                    pk[e] = pack_bf16(exp2_approx(t0), exp2_approx(t1));
                     // the row sum adds the bf16 values PV multiplies, so the
                     // output is an exactly normalised average of the values
-                    psum += bf16_lo(pk[e]) + bf16_hi(pk[e]);
+                    add_bf16_pair(s0, s1, pk[e]);
                 }
+                const float psum = s0 + s1;
                 tmem_st16u(tmem + lane_off + kSCol + (j & 1) * kBlockN + q * (SW / 2), pk);
                 tmem_wait_st();
                 l += psum;
