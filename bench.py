@@ -443,7 +443,7 @@ def measure_projection(dev, iters=50, warmup=5):
     return out
 
 
-def measure_attention_workloads(dev, iters=20, warmup=3):
+def measure_attention_workloads(dev, iters=20, warmup=3, names=None):
     """medusa_tree_attention alone at the other workloads' shapes: batch 8 of
     the 13B shape (40 heads, ragged KV lengths 1024..4096, sparse tree) and
     batch 4 at KV 8192 with the sparse 64-node and the dense 341-node trees.
@@ -463,6 +463,8 @@ def measure_attention_workloads(dev, iters=20, warmup=3):
     D = 128
     out = {}
     for name, paths, maxd, B, Hq, lens in cases:
+        if names is not None and name not in names:
+            continue
         t = M.tree_layout(paths, maxd)
         N = t["N"]
         Lmax = int(lens.max()) + N
@@ -1161,6 +1163,10 @@ def main():
                          "5 heads, top-8, bf16, random-init weights) --steps times, print the last "
                          "call's time, and exit")
     ap.add_argument("--hidden", type=int, default=4096)
+    ap.add_argument("--only-attention", default="", metavar="NAME",
+                    choices=["", "13b_b8_ragged_sparse64", "b4_kv8192_sparse64", "b4_kv8192_dense341"],
+                    help="profiling aid: run medusa_tree_attention at one of the attention workloads' "
+                         "shapes, --warmup then --steps calls, print the time per call, and exit")
     ap.add_argument("--only-step", action="store_true",
                     help="profiling aid: run --warmup then --steps steps of --workload, print their time, and exit")
     ap.add_argument("--workload", default="h4096_b1_sparse64",
@@ -1172,6 +1178,13 @@ def main():
         args.warmup = 3
     if args.only_heads:
         return only_heads(args.only_heads, args.hidden, args.steps)
+    if args.only_attention:
+        import torch
+        res = measure_attention_workloads(torch.device("cuda", 0), iters=args.steps, warmup=args.warmup,
+                                          names=[args.only_attention])
+        print(json.dumps({"only_attention": args.only_attention, "calls": args.steps,
+                          **{k: res[args.only_attention][k] for k in ("us", "frac_hbm", "frac_bf16")}}))
+        return 0
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -66,6 +66,34 @@ __device__ __forceinline__ void add_bf16_pair(float& s0, float& s1, uint32_t w) 
         : "+f"(s0), "+f"(s1) : "r"(w));
 }
 
+// Visibility of keys c0 .. c0 + 31 to one query row, as a bit mask (bit e: key
+// c0 + e): the key lies in [klo, k_end) and, if it is a tree key (>= Lb), the
+// row's ancestor mask holds its tree position; prefix keys are visible to every
+// row.  The mask row's bits for the chunk are taken with one funnel shift.
+__device__ __forceinline__ uint32_t key_visibility32(int c0, int klo, int k_end, int Lb, bool valid,
+                                                     const uint64_t* mrow, int W) {
+    uint32_t vm = 0xffffffffu;
+    const int lo = klo - c0;  // bits below lo: keys before the range
+    if (lo > 0) vm = lo >= 32 ? 0u : vm & (0xffffffffu << lo);
+    const int hi = k_end - c0;  // bits from hi on: keys past its end
+    if (hi < 32) vm = hi <= 0 ? 0u : vm & (0xffffffffu >> (32 - hi));
+    const int off = c0 - Lb;  // tree position of bit 0 (negative: prefix keys come first)
+    if (off > -32) {
+        uint32_t tree = 0;
+        if (valid) {
+            const int p = max(off, 0);  // first tree position in the chunk
+            const int wi = p >> 6, sh = p & 63;
+            const uint64_t w0 = wi < W ? __ldg(mrow + wi) : 0ull;
+            const uint64_t w1 = wi + 1 < W ? __ldg(mrow + wi + 1) : 0ull;
+            const uint64_t bits = sh ? (w0 >> sh) | (w1 << (64 - sh)) : w0;  // bit j: position p + j
+            tree = off >= 0 ? (uint32_t)bits : (uint32_t)(bits << (-off));
+        }
+        const uint32_t prefix = off >= 0 ? 0u : 0xffffffffu >> (32 + off);  // bits below -off
+        vm &= prefix | tree;
+    }
+    return vm;
+}
+
 struct AttnArgs {
     const uint16_t* q;
     const uint16_t* k;
@@ -425,24 +453,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
                     }
                     mt = fmaxf(m0, m1);
                 } else {
-                    uint64_t w0 = 0, w1 = 0;
-                    int mbase = 0;
-                    if (valid && c0 + SW > Lb) {
-                        mbase = max(c0 - Lb, 0) & ~63;
-                        const int wi = mbase >> 6;
-                        w0 = wi < a.W ? __ldg(mrow + wi) : 0ull;
-                        w1 = wi + 1 < a.W ? __ldg(mrow + wi + 1) : 0ull;
-                    }
+                    const uint32_t vm = key_visibility32(c0, klo, k_end, Lb, valid, mrow, a.W);
 #pragma unroll
-                    for (int i = 0; i < SW; ++i) {
-                        const int key = c0 + i;
-                        bool vis = key >= klo && key < k_end;
-                        if (key >= Lb) {
-                            const int m = key - Lb - mbase;  // in [0, 96)
-                            vis = vis && valid && (((m < 64 ? w0 >> m : w1 >> (m - 64)) & 1ull) != 0);
-                        }
-                        sv[i] = vis ? sv[i] : -INFINITY;
-                        mt = fmaxf(mt, sv[i]);
+                    for (int i = 0; i < SW; i += 2) {
+                        sv[i] = (vm >> i) & 1u ? sv[i] : -INFINITY;
+                        sv[i + 1] = (vm >> (i + 1)) & 1u ? sv[i + 1] : -INFINITY;
+                        mt = fmax3(mt, sv[i], sv[i + 1]);
                     }
                 }
                 // raw scores are scaled inside the exponent's FMA below; the
@@ -626,6 +642,410 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
     }
 }
 
+// ---------------------------------------------------------------------------
+// Two-stream tcgen05 kernel, for query blocks of more than 64 rows whose keys
+// are not split across CTAs.  The block's key tiles are cut in two halves, each
+// an independent online softmax (a "stream") with its own TMEM accumulator O_s
+// and score buffer S_s; the two partial results are merged at the end.  The
+// tensor core alternates between the streams, so one stream's softmax runs
+// while the other's MMAs do, and each softmax thread owns a whole query row:
+// no row statistic crosses threads inside the tile loop.
+//
+// Warp roles (320 threads):
+//   warps 0-3, 4-7  softmax of stream 0, 1: thread r of the warpgroup owns TMEM
+//                   lane r (block row r), all 128 scores of each of its
+//                   stream's tiles, and half of the row's output columns
+//   warp 8          MMA: lane 0 issues every tcgen05.mma and commit
+//   warp 9          TMA: lane 0 loads Q and streams K and V tiles into two
+//                   3-deep rings in the order the MMAs consume them
+// Tiles are consumed in the order u = 0, 1, 2, ...; u = 2i + s is stream s's
+// tile i (key tile i for s = 0, key tile nA + i for s = 1, nA = ceil(tiles/2)).
+// TMEM (512 columns): O_0 at 0, O_1 at 128, S_0 at 256, S_1 at 384; P_s is
+// written as bf16 over the first 64 columns of S_s.  For u = 0, 1, 2, ... the
+// MMA lane issues PV(u) and then S(u + 2), so the commit of S_s(i) also covers
+// PV_s(i - 1): a stream's softmax may rescale O_s once its scores are in.
+// Every wait is bounded; a CTA that gives up writes NaN.
+// ---------------------------------------------------------------------------
+constexpr int kDualThreads = 320;
+constexpr int kDualSoftmaxWarps = 8;
+constexpr int kDualMmaWarp = 8, kDualTmaWarp = 9;
+constexpr int kDualRing = 3;
+
+template <int D>
+struct DualSmem {
+    static constexpr int kQ = kUmmaM * D * 2;
+    static constexpr int kTile = kBlockN * D * 2;  // one K or V tile
+    static constexpr int kOffK = kQ;
+    static constexpr int kOffV = kOffK + kDualRing * kTile;
+    static constexpr int kOffBar = kOffV + kDualRing * kTile;
+    // kfull[R] vfull[R] kempty[R] vempty[R] s_full[2] o_done[2] p_full[2] qfull drain
+    static constexpr int kNumBar = 4 * kDualRing + 8;
+    static constexpr int kOffMisc = kOffBar + kNumBar * 8;  // tmem slot, flag
+    static constexpr int kBytes = kOffMisc + 16 + 1024;     // + alignment slack
+    // after the tile loop the K ring holds the streams' row statistics,
+    // float (max, sum) [2][128]
+    static_assert(2 * kUmmaM * 2 * 4 <= kDualRing * kTile, "row statistics fit the K ring");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kDualThreads, 1) tree_attn_dual_kernel(
+    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+    const __grid_constant__ CUtensorMap tmq, AttnArgs a) {
+    using namespace umma;
+    using L = DualSmem<D>;
+    constexpr int CH = D / 8;  // 16-byte chunks per row
+    constexpr int TMEM_COLS = 512;
+    constexpr uint32_t kOCol = 128, kSCol = 256;  // O_s at 128 s, S_s at 256 + 128 s
+    constexpr int R = kDualRing;
+    extern __shared__ uint8_t smem_raw[];
+
+    const int hk = blockIdx.y / a.qblocks, qb = blockIdx.y % a.qblocks;
+    const int N = a.N, G = a.G;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = tid & (kUmmaM - 1);
+    const int strm = (warp >> 2) & 1;  // stream of a softmax warp
+
+    const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+    uint8_t* base = smem_raw + pad;
+    const uint32_t base_a = smem_addr(base);
+    const uint32_t qs_a = base_a, ks_a = base_a + L::kOffK, vs_a = base_a + L::kOffV;
+    const uint32_t bar_a = base_a + L::kOffBar;
+    const uint32_t kfull0 = bar_a, vfull0 = kfull0 + 8 * R, kempty0 = vfull0 + 8 * R, vempty0 = kempty0 + 8 * R,
+                   s_full0 = vempty0 + 8 * R, o_done0 = s_full0 + 16, p_full0 = o_done0 + 16,
+                   qfull = p_full0 + 16, drain = qfull + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kOffMisc);
+    volatile int* flag = reinterpret_cast<volatile int*>(base + L::kOffMisc + 4);
+    const long long lim = g_wait_limit;
+    bool q_issued = false;
+    int issued_k = 0, issued_v = 0;
+
+    if (warp == kDualTmaWarp && lane == 0) {
+        for (int i = 0; i < L::kNumBar; ++i) mbar_init(bar_a + 8 * i, 1);
+        mbar_init(p_full0, 4);
+        mbar_init(p_full0 + 8, 4);
+        mbar_init_fence();
+        *flag = 0;
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+        if (a.q_tma) prefetch_tmap(&tmq);
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
+    pdl_wait();
+    pdl_trigger();
+    // sequences longest first (blockIdx.z is a rank by decreasing KV length)
+    __shared__ int s_seq;
+    int b = blockIdx.z;
+    if (a.B > 1 && a.B <= kDualThreads) {
+        const int t = threadIdx.x;
+        if (t < a.B) {
+            const int Lt = clamp_len(a.kv_len[t], N, a.Lmax);
+            int rank = 0;
+            for (int j = 0; j < a.B; ++j) {
+                const int Lj = clamp_len(a.kv_len[j], N, a.Lmax);
+                rank += (Lj > Lt || (Lj == Lt && j < t)) ? 1 : 0;
+            }
+            if (rank == (int)blockIdx.z) s_seq = t;
+        }
+        __syncthreads();
+        b = s_seq;
+    }
+    const int Lb = clamp_len(a.kv_len[b], N, a.Lmax);
+    const int k_end = Lb + N;  // every key of the sequence: prefix, then the tree
+    const int ntiles = (k_end + kBlockN - 1) / kBlockN;
+    const int nA = (ntiles + 1) / 2, nB = ntiles / 2;
+    const int rows = N * G;
+    const int row0 = qb * kUmmaM;
+    const int nblk = min(rows - row0, kUmmaM);
+    auto tile_lo = [&](int t) { return t * kBlockN; };
+    auto tile_start = [&](int t) { return min(t * kBlockN, k_end - kBlockN); };
+    auto key_tile = [&](int u) { return (u & 1) ? nA + (u >> 1) : (u >> 1); };
+    const int zrow = b * a.Hkv + hk;
+
+    if (warp == kDualTmaWarp && lane == 0) {
+        if (a.q_tma && ntiles > 0) {
+            q_issued = true;
+            mbar_expect_tx(qfull, L::kQ);
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x)
+                tma_load_4d(qs_a + x * kUmmaM * 128, &tmq, x * 64, hk * G, row0 / G, b, qfull);
+        }
+        for (int u = 0; u < R && u < ntiles; ++u) {
+            issued_k = issued_v = u + 1;
+            mbar_expect_tx(kfull0 + 8 * u, L::kTile);
+            mbar_expect_tx(vfull0 + 8 * u, L::kTile);
+            const int ks = tile_start(key_tile(u));
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x) {
+                tma_load_3d(ks_a + u * L::kTile + x * kBlockN * 128, &tmk, x * 64, ks, zrow, kfull0 + 8 * u);
+                tma_load_3d(vs_a + u * L::kTile + x * kBlockN * 128, &tmv, x * 64, ks, zrow, vfull0 + 8 * u);
+            }
+        }
+    }
+    // Q tile without TMA (group size not dividing 128); padding rows are zero
+    if (!a.q_tma && warp < kDualSoftmaxWarps) {
+        for (int c = tid; c < kUmmaM * CH; c += kDualSoftmaxWarps * 32) {
+            const int m = c / CH, ch = c % CH;
+            const bool ok = m < nblk;
+            const int gr = row0 + (ok ? m : 0);
+            const int node = gr / G, hq = hk * G + gr % G;
+            cp_async16(qs_a + sw128_offset(m, ch, kUmmaM),
+                       a.q + (((size_t)b * N + (ok ? node : 0)) * a.Hq + (ok ? hq : 0)) * D + ch * 8, ok);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_async_smem();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    float m_ref = -INFINITY, l = 0.f;
+    bool gave_up = false;
+    if (warp == kDualMmaWarp) {
+        // -------------------------------- MMA lane --------------------------------
+        if (lane == 0 && ntiles > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(kUmmaM, kBlockN, 0, 0);
+            constexpr uint32_t idesc_pv = idesc_bf16(kUmmaM, D, 0, 1);
+            const uint64_t dq0 = desc_sw128(qs_a, 16, 1024);
+            const uint64_t dk0 = desc_sw128(ks_a, 16, 1024);
+            const uint64_t dv0 = desc_sw128(vs_a, kBlockN * 128, 1024);
+            bool fail = false;
+            auto wait = [&](uint32_t bar, uint32_t parity) {
+                if (fail) return false;
+                if (!mbar_wait(bar, parity, lim)) { fail = true; *flag = 1; return false; }
+                return true;
+            };
+            auto issue_s = [&](int u) {  // S_s(i) = Q K_u^T into S buffer s = u & 1
+                const uint64_t dk = dk0 + (uint64_t)(((u % R) * L::kTile) >> 4);
+                const uint32_t d = tmem + kSCol + (u & 1) * 128;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t qo = ((ks >> 2) * (kUmmaM * 128) + (ks & 3) * 32) >> 4;
+                    const uint32_t ko = ((ks >> 2) * (kBlockN * 128) + (ks & 3) * 32) >> 4;
+                    mma_bf16(d, dq0 + qo, dk + ko, idesc_s, ks > 0);
+                }
+                commit(s_full0 + 8 * (u & 1));
+                commit(kempty0 + 8 * (u % R));
+            };
+            auto issue_pv = [&](int u) {  // O_s += P_s(i) V_u
+                const int s = u & 1, i = u >> 1;
+                const uint64_t dv = dv0 + (uint64_t)(((u % R) * L::kTile) >> 4);
+                const uint32_t pa = tmem + kSCol + s * 128;
+#pragma unroll
+                for (int ks = 0; ks < kBlockN / 16; ++ks)
+                    mma_bf16_ta(tmem + s * kOCol, pa + ks * 8, dv + ((ks * 2048) >> 4), idesc_pv,
+                                (i > 0 || ks > 0) ? 1u : 0u);
+                if (u + 2 >= ntiles) commit(o_done0 + 8 * s);  // the stream's last PV
+                commit(vempty0 + 8 * (u % R));
+            };
+            if (!a.q_tma || wait(qfull, 0))
+                for (int u = 0; u < 2 && u < ntiles; ++u) {
+                    if (!wait(kfull0 + 8 * (u % R), (uint32_t)((u / R) & 1))) break;
+                    issue_s(u);
+                }
+            for (int u = 0; u < ntiles && !fail; ++u) {
+                if (!wait(p_full0 + 8 * (u & 1), (uint32_t)((u >> 1) & 1))) break;
+                if (!wait(vfull0 + 8 * (u % R), (uint32_t)((u / R) & 1))) break;
+                fence_after_sync();
+                issue_pv(u);
+                if (u + 2 < ntiles) {
+                    if (!wait(kfull0 + 8 * ((u + 2) % R), (uint32_t)(((u + 2) / R) & 1))) break;
+                    issue_s(u + 2);
+                }
+            }
+        }
+    } else if (warp == kDualTmaWarp) {
+        // -------------------------------- TMA lane --------------------------------
+        if (lane == 0) {
+            for (int u = R; u < ntiles; ++u) {
+                // stage u % R held tile u - R: wait for the MMAs that read it
+                const uint32_t par = (uint32_t)((u / R - 1) & 1);
+                const int ks = tile_start(key_tile(u));
+                if (!mbar_wait(kempty0 + 8 * (u % R), par, lim)) { *flag = 1; break; }
+                mbar_expect_tx(kfull0 + 8 * (u % R), L::kTile);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+                    tma_load_3d(ks_a + (u % R) * L::kTile + x * kBlockN * 128, &tmk, x * 64, ks, zrow,
+                                kfull0 + 8 * (u % R));
+                issued_k = u + 1;
+                if (!mbar_wait(vempty0 + 8 * (u % R), par, lim)) { *flag = 1; break; }
+                mbar_expect_tx(vfull0 + 8 * (u % R), L::kTile);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+                    tma_load_3d(vs_a + (u % R) * L::kTile + x * kBlockN * 128, &tmv, x * 64, ks, zrow,
+                                vfull0 + 8 * (u % R));
+                issued_v = u + 1;
+            }
+        }
+    } else {
+        // ------------------------------ softmax warps ------------------------------
+        const int s = strm;
+        const int ns = s ? nB : nA;
+        const bool valid = r < nblk;
+        const bool warp_valid = __any_sync(0xffffffffu, valid);
+        const int grow = row0 + (valid ? r : 0);
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_off + kSCol + s * 128, tO = tmem + lane_off + s * kOCol;
+        const uint64_t* mrow = a.mask + (size_t)(grow / G) * a.W;
+        bool fail = false;
+        for (int i = 0; i < ns; ++i) {
+            bool ok = mbar_wait(s_full0 + 8 * s, (uint32_t)(i & 1), lim);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) { fail = true; break; }
+            fence_after_sync();
+            if (warp_valid) {
+                const int t = s ? nA + i : i;
+                const int kt = tile_start(t), klo = tile_lo(t);
+                float sv[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sv[c]);
+                tmem_wait_ld();
+                float mt;
+                if (kt == klo && kt + kBlockN <= min(k_end, Lb)) {  // plain prefix tile
+                    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            m0 = fmax3(m0, sv[c][e], sv[c][e + 1]);
+                            m1 = fmax3(m1, sv[c][e + 2], sv[c][e + 3]);
+                        }
+                    mt = fmaxf(m0, m1);
+                } else {
+                    mt = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t vm = key_visibility32(kt + 32 * c, klo, k_end, Lb, valid, mrow, a.W);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            sv[c][e] = (vm >> e) & 1u ? sv[c][e] : -INFINITY;
+                            sv[c][e + 1] = (vm >> (e + 1)) & 1u ? sv[c][e + 1] : -INFINITY;
+                            mt = fmax3(mt, sv[c][e], sv[c][e + 1]);
+                        }
+                    }
+                }
+                // raw scores are scaled inside the exponent's FMA below; the
+                // scale is positive, so the row maximum scales the same way
+                mt *= a.scale_log2;
+                float corr = 1.f;
+                bool rescale = false;
+                if (mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleThreshold)) {
+                    if (m_ref != -INFINITY) { corr = exp2f(m_ref - mt); rescale = true; }
+                    m_ref = mt;
+                }
+                const float mr = m_ref == -INFINITY ? 0.f : m_ref;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float t0, t1;
+                        fma_pair(sv[c][2 * e], sv[c][2 * e + 1], a.scale_log2, -mr, t0, t1);
+                        pk[e] = pack_bf16(exp2_approx(t0), exp2_approx(t1));
+                        // the row sum adds the bf16 values PV multiplies
+                        add_bf16_pair(s0, s1, pk[e]);
+                    }
+                    tmem_st16u(tS + 16 * c, pk);
+                }
+                l = l * corr + (s0 + s1);
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O_s holds PV_s(i - 1): its commit preceded this tile's scores
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        float ov[32];
+                        tmem_ld32(tO + 32 * c, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ov[e] *= corr;
+                        tmem_st32(tO + 32 * c, ov);
+                    }
+                }
+                tmem_wait_st();
+            }
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full0 + 8 * s);
+        }
+        bool ok = !fail;
+        if (ok && ns > 0) ok = mbar_wait(o_done0 + 8 * s, 0, lim);
+        gave_up = !ok;
+    }
+    bool bad = __syncthreads_or(gave_up);
+    bad = bad || *flag != 0;  // every write to the flag precedes the barrier
+    if (bad) {
+        // Gave up: let everything this CTA started complete before its tensor
+        // memory is freed and it leaves (default-limit waits).
+        if (warp == kDualMmaWarp && lane == 0) {
+            commit(drain);
+            mbar_wait(drain, 0, kWaitCycles);
+        }
+        if (warp == kDualTmaWarp && lane == 0) {
+            if (q_issued) mbar_wait(qfull, 0, kWaitCycles);
+            for (int u = max(0, issued_k - R); u < issued_k; ++u)
+                mbar_wait(kfull0 + 8 * (u % R), (uint32_t)((u / R) & 1), kWaitCycles);
+            for (int u = max(0, issued_v - R); u < issued_v; ++u)
+                mbar_wait(vfull0 + 8 * (u % R), (uint32_t)((u / R) & 1), kWaitCycles);
+        }
+        if (tid == 0) atomicExch(&g_wait_gave_up, 1);
+    }
+
+    // ------------------------------ epilogue ------------------------------
+    // The streams swap (max, sum) through the K ring, free now: every MMA
+    // completed (both streams' last commits were waited for) and every tile
+    // that landed was consumed.
+    float* xch = reinterpret_cast<float*>(base + L::kOffK);
+    if (warp < kDualSoftmaxWarps && !bad) {
+        xch[2 * (strm * kUmmaM + r)] = m_ref;
+        xch[2 * (strm * kUmmaM + r) + 1] = l;
+    }
+    __syncthreads();
+    if (warp < kDualSoftmaxWarps && ntiles > 0) {
+        const bool valid = r < nblk;
+        const int grow = row0 + (valid ? r : 0);
+        const int node = grow / G, hq = hk * G + grow % G;
+        float* dst = a.out + (((size_t)b * N + node) * a.Hq + hq) * D + strm * (D / 2);
+        if (bad) {
+            if (valid)
+                for (int e = 0; e < D / 2; e += 4)
+                    *reinterpret_cast<float4*>(dst + e) = make_float4(NAN, NAN, NAN, NAN);
+        } else if (__any_sync(0xffffffffu, valid)) {
+            const float mA = xch[2 * r], lA = xch[2 * r + 1];
+            const float mB = xch[2 * (kUmmaM + r)], lB = xch[2 * (kUmmaM + r) + 1];
+            const float mx = fmaxf(lA > 0.f ? mA : -INFINITY, lB > 0.f ? mB : -INFINITY);
+            const float mb = mx == -INFINITY ? 0.f : mx;
+            const float wA = lA > 0.f ? exp2f(mA - mb) : 0.f, wB = lB > 0.f ? exp2f(mB - mb) : 0.f;
+            const float den = lA * wA + lB * wB;
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            const float cA = wA * inv, cB = wB * inv;
+            const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+#pragma unroll 1
+            for (int c = 0; c < D / 64; ++c) {
+                const uint32_t col = strm * (D / 2) + 32 * c;
+                float oa[32], ob[32];
+                tmem_ld32(tmem + lane_off + col, oa);
+                if (nB > 0) tmem_ld32(tmem + lane_off + kOCol + col, ob);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        float4 o;
+                        o.x = oa[e] * cA + (cB > 0.f ? ob[e] * cB : 0.f);
+                        o.y = oa[e + 1] * cA + (cB > 0.f ? ob[e + 1] * cB : 0.f);
+                        o.z = oa[e + 2] * cA + (cB > 0.f ? ob[e + 2] * cB : 0.f);
+                        o.w = oa[e + 3] * cA + (cB > 0.f ? ob[e + 3] * cB : 0.f);
+                        *reinterpret_cast<float4*>(dst + 32 * c + e) = o;
+                    }
+                }
+            }
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
 // float32 storage: one warp per (b, node, query head), keys in order, online softmax.
 template <int D>
 __global__ void __launch_bounds__(256) tree_attn_f32_kernel(const float* __restrict__ q,
@@ -773,6 +1193,24 @@ int launch_bf16(AttnArgs& a, const AttnPlan& p, cudaStream_t st) {
         if (rc) return rc;
     } else {
         tmq = tmk;  // unused
+    }
+    if (p.S == 1 && !a.spread && (size_t)DualSmem<D>::kBytes <= (size_t)max_smem_optin()) {
+        // blocks of more than 64 rows with unsplit keys: two streams per CTA
+        auto kern = tree_attn_dual_kernel<D>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DualSmem<D>::kBytes);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, a.Hkv * p.qblocks, a.B);
+        cfg.blockDim = dim3(kDualThreads);
+        cfg.dynamicSmemBytes = DualSmem<D>::kBytes;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmk, tmv, tmq, a);
+        if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "tree_attention: launch failed: %s", cudaGetErrorString(e));
+        return MEDUSA_OK;
     }
     auto kern = tree_attn_umma_kernel<D>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);

@@ -73,6 +73,12 @@ def test_attention_full_compare(medusa, kind, B, Hq, Hkv, D, lens, Lmax, dtype):
     ("dense", 2, 38, 38, 128, [100, 300], 700),
     ("dense", 2, 38, 38, 64, [0, 250], 600),
     ("max512", 1, 76, 38, 64, [129], 650),
+    # two-stream kernel (blocks of more than 64 rows, keys not split): one key
+    # tile (the second stream empty), two and three tiles, and a group size of
+    # 3 (query rows gathered without TMA)
+    ("small", 4, 152, 38, 64, [0, 5, 108, 60], 128),
+    ("small", 4, 152, 38, 128, [0, 200, 108, 350], 370),
+    ("dense", 1, 156, 52, 64, [300], 700),
 ])
 def test_attention_many_blocks(medusa, kind, B, Hq, Hkv, D, lens, Lmax):
     t = _tree(kind)
