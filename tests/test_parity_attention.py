@@ -79,6 +79,9 @@ def test_attention_full_compare(medusa, kind, B, Hq, Hkv, D, lens, Lmax, dtype):
     ("small", 4, 152, 38, 64, [0, 5, 108, 60], 128),
     ("small", 4, 152, 38, 128, [0, 200, 108, 350], 370),
     ("dense", 1, 156, 52, 64, [300], 700),
+    # two-stream kernel over ragged lengths of 1 to 9 key tiles (single-tile
+    # blocks leave the second stream empty) in more blocks than SMs
+    ("small", 4, 160, 40, 128, [0, 300, 5, 1000], 1100),
 ])
 def test_attention_many_blocks(medusa, kind, B, Hq, Hkv, D, lens, Lmax):
     t = _tree(kind)
