@@ -318,70 +318,102 @@ def _pack(tensors, device, pinned=False):
     return buf, views
 
 
-def run_e2e(step, steps, warmup):
+def run_e2e(step, steps, warmup, pipelined=True):
     """Same step through the C ABI with host buffers: per-step inputs copied from
     pinned host memory, results read back, all inside the timed region.  Every
     input (h, q, verifier logits, tree hidden states, the tree's K/V rows)
     travels in one packed host-to-device copy and the results in one packed
     read; the tree's K/V rows then move from the staging buffer into their
-    cache slots on the device.  The whole step (copies and calls) is one CUDA
-    graph replayed and waited for once per step."""
+    cache slots on the device.  The copy and the step (its K/V placement, five
+    calls and result read) are CUDA graphs.
+
+    pipelined: two staging buffers; step k + 1's inputs are copied on a copy
+    stream while step k computes, and the host waits for step k's results
+    right after enqueuing step k + 1 (two steps in flight, as a serving loop
+    with a prefetching input queue runs).  Otherwise every step copies, computes
+    and is waited for before the next starts."""
     torch = step.torch
     L = int(step.kv_len0[0].item())
     N = step.N
     dev = step.h.device
-    # inputs: one device staging buffer (the step reads h, q, logits and hidden
-    # states from it; the K/V rows are copied on to the cache) and its pinned twin
+    nbuf = 2 if pipelined else 1
     names_in = ("h", "q", "vlogits", "ht")
     tree_kv = [step.kc[:, :, L:L + N].contiguous(), step.vc[:, :, L:L + N].contiguous()]
-    dbuf_in, views = _pack([getattr(step, n) for n in names_in] + tree_kv, dev)
-    for n, v in zip(names_in, views):
-        setattr(step, n, v)
-    tk, tv = views[4], views[5]
-    hbuf_in, _ = _pack([getattr(step, n).cpu() for n in names_in] + [t.cpu() for t in tree_kv], "cpu",
-                       pinned=True)
-    # results: the step writes them into one device buffer, read back in one copy
+    src = [getattr(step, n) for n in names_in] + tree_kv
+    staged = [_pack(src, dev) for _ in range(nbuf)]  # (device buffer, views) per slot
+    hbuf_in, _ = _pack([t.cpu() for t in src], "cpu", pinned=True)
     names_out = ("accept_len", "best_node", "path_nodes", "next_tok")
     dbuf_out, outs = _pack([step.acc[n] for n in names_out] + [step.h_next], dev)
     for n, v in zip(names_out, outs[:4]):
         step.acc[n] = v
     step.h_next = outs[4]
-    hbuf_out = torch.empty(dbuf_out.numel(), dtype=torch.uint8).pin_memory()
+    hbuf_out = [torch.empty(dbuf_out.numel(), dtype=torch.uint8).pin_memory() for _ in range(nbuf)]
     h2d = hbuf_in.numel()
-    d2h = hbuf_out.numel()
+    d2h = dbuf_out.numel()
 
-    def enqueue():
-        dbuf_in.copy_(hbuf_in, non_blocking=True)
-        step.kc[:, :, L:L + N].copy_(tk)
-        step.vc[:, :, L:L + N].copy_(tv)
+    def enqueue_copy(p):
+        staged[p][0].copy_(hbuf_in, non_blocking=True)
+
+    def enqueue_step(p):
+        views = staged[p][1]
+        for n, v in zip(names_in, views):
+            setattr(step, n, v)
+        step.kc[:, :, L:L + N].copy_(views[4])
+        step.vc[:, :, L:L + N].copy_(views[5])
         step.run()
-        hbuf_out.copy_(dbuf_out, non_blocking=True)
+        hbuf_out[p].copy_(dbuf_out, non_blocking=True)
 
-    # The step is captured once as a CUDA graph (the copies from and to pinned
-    # host memory, the five calls); each timed step replays it and waits for it,
-    # so every step still moves its inputs in and its results out.
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        for _ in range(2):
-            enqueue()
+    cs, ss = torch.cuda.Stream(), torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    ss.wait_stream(torch.cuda.current_stream())
+    for p in range(nbuf):  # warm-up before capture
+        with torch.cuda.stream(cs):
+            enqueue_copy(p)
+        ss.wait_stream(cs)
+        with torch.cuda.stream(ss):
+            enqueue_step(p)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        enqueue()
+    gc, gs = [], []
+    for p in range(nbuf):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            enqueue_copy(p)
+        gc.append(g)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=ss):
+            enqueue_step(p)
+        gs.append(g)
+    copied = [torch.cuda.Event() for _ in range(nbuf)]
+    done = [torch.cuda.Event() for _ in range(nbuf)]
 
-    def one():
-        g.replay()
-        torch.cuda.current_stream().synchronize()
+    def launch(k):
+        p = k % nbuf
+        with torch.cuda.stream(cs):
+            if k >= nbuf:
+                cs.wait_event(done[p])  # slot p was read by step k - nbuf
+            gc[p].replay()
+            copied[p].record(cs)
+        with torch.cuda.stream(ss):
+            ss.wait_event(copied[p])
+            gs[p].replay()
+            done[p].record(ss)
 
-    for _ in range(warmup):
-        one()
+    def run(n):
+        for k in range(n):
+            launch(k)
+            if pipelined:
+                if k >= 1:
+                    done[(k - 1) % nbuf].synchronize()  # step k - 1's results are on the host
+            else:
+                done[0].synchronize()
+        done[(n - 1) % nbuf].synchronize()
+
+    run(max(warmup, 2))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
-    torch.cuda.synchronize()
+    run(steps)
     dt = time.perf_counter() - t0
+    torch.cuda.synchronize()
     return dt, h2d, d2h
 
 
@@ -1294,8 +1326,10 @@ def main():
     ms_step = ms_total / K
     value = replica_throughput(K, ms_total, world)
 
-    e2e_s, h2d, d2h = run_e2e(step, max(20, K // 4), args.warmup)
-    e2e_val = world * max(20, K // 4) / e2e_s
+    ke = max(20, K // 4)
+    e2e_serial_s, _, _ = run_e2e(step, ke, args.warmup, pipelined=False)
+    e2e_s, h2d, d2h = run_e2e(step, ke, args.warmup, pipelined=True)
+    e2e_val = world * ke / e2e_s
 
     lead = world == 1 or rank == 0
     graph = measure_step_graph(step) if lead else None
@@ -1340,7 +1374,12 @@ def main():
             "heads_batches": heads_b,
             "clocks": clocks,
             "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "pipeline": "two steps in flight: the next step's inputs are copied from pinned host "
+                                "memory on a copy stream while the current step computes; every step's "
+                                "results are read back and waited for by the host"},
+            "e2e_serial": {"value": world * ke / e2e_serial_s, "unit": "steps/s",
+                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": step.launches * K}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp)
