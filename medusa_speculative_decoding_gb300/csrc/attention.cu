@@ -643,10 +643,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) tree_attn_umma_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Two-stream tcgen05 kernel, for query blocks of more than 64 rows whose keys
-// are not split across CTAs.  The block's key tiles are cut in two halves, each
-// an independent online softmax (a "stream") with its own TMEM accumulator O_s
-// and score buffer S_s; the two partial results are merged at the end.  The
+// Two-stream tcgen05 kernel, for query blocks whose keys are not split across
+// CTAs (a block of at most 64 query rows is spread 16 rows per TMEM lane
+// quarter, as in the cluster kernel).  The block's key tiles are cut in two
+// halves, each an independent online softmax (a "stream") with its own TMEM
+// accumulator O_s and score buffer S_s; the two partial results are merged at
+// the end.  The
 // tensor core alternates between the streams, so one stream's softmax runs
 // while the other's MMAs do, and each softmax thread owns a whole query row:
 // no row statistic crosses threads inside the tile loop.
@@ -756,6 +758,15 @@ __global__ void __launch_bounds__(kDualThreads, 1) tree_attn_dual_kernel(
     const int rows = N * G;
     const int row0 = qb * kUmmaM;
     const int nblk = min(rows - row0, kUmmaM);
+    // A block of at most 64 rows is spread 16 rows per TMEM lane quarter, so
+    // all four SM sub-partitions share the softmax; otherwise block row i is
+    // TMEM lane i.
+    const bool spread = a.spread != 0;
+    auto qrow_of = [&](int m) -> int {  // TMEM lane -> block row, -1 for padding
+        const int i = spread ? (((m & 31) < 16) ? 16 * (m >> 5) + (m & 15) : -1) : m;
+        return (i >= 0 && i < nblk) ? i : -1;
+    };
+    // the last tile ends at the last key (keys it brings back are masked)
     auto tile_lo = [&](int t) { return t * kBlockN; };
     auto tile_start = [&](int t) { return min(t * kBlockN, k_end - kBlockN); };
     auto key_tile = [&](int u) { return (u & 1) ? nA + (u >> 1) : (u >> 1); };
@@ -764,10 +775,20 @@ __global__ void __launch_bounds__(kDualThreads, 1) tree_attn_dual_kernel(
     if (warp == kDualTmaWarp && lane == 0) {
         if (a.q_tma && ntiles > 0) {
             q_issued = true;
-            mbar_expect_tx(qfull, L::kQ);
+            if (spread) {  // block rows 16g .. 16g+15 -> TMEM lanes 32g .. 32g+15
+                mbar_expect_tx(qfull, 4 * 16 * D * 2);
 #pragma unroll
-            for (int x = 0; x < D / 64; ++x)
-                tma_load_4d(qs_a + x * kUmmaM * 128, &tmq, x * 64, hk * G, row0 / G, b, qfull);
+                for (int x = 0; x < D / 64; ++x)
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        tma_load_4d(qs_a + x * kUmmaM * 128 + g * 32 * 128, &tmq, x * 64, hk * G,
+                                    (row0 + 16 * g) / G, b, qfull);
+            } else {
+                mbar_expect_tx(qfull, L::kQ);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+                    tma_load_4d(qs_a + x * kUmmaM * 128, &tmq, x * 64, hk * G, row0 / G, b, qfull);
+            }
         }
         for (int u = 0; u < R && u < ntiles; ++u) {
             issued_k = issued_v = u + 1;
@@ -784,9 +805,10 @@ __global__ void __launch_bounds__(kDualThreads, 1) tree_attn_dual_kernel(
     // Q tile without TMA (group size not dividing 128); padding rows are zero
     if (!a.q_tma && warp < kDualSoftmaxWarps) {
         for (int c = tid; c < kUmmaM * CH; c += kDualSoftmaxWarps * 32) {
-            const int m = c / CH, ch = c % CH;
-            const bool ok = m < nblk;
-            const int gr = row0 + (ok ? m : 0);
+            const int m = c / CH, ch = c % CH;  // TMEM lane m = MMA row m
+            const int i = qrow_of(m);
+            const bool ok = i >= 0;
+            const int gr = row0 + max(i, 0);
             const int node = gr / G, hq = hk * G + gr % G;
             cp_async16(qs_a + sw128_offset(m, ch, kUmmaM),
                        a.q + (((size_t)b * N + (ok ? node : 0)) * a.Hq + (ok ? hq : 0)) * D + ch * 8, ok);
@@ -882,9 +904,10 @@ __global__ void __launch_bounds__(kDualThreads, 1) tree_attn_dual_kernel(
         // ------------------------------ softmax warps ------------------------------
         const int s = strm;
         const int ns = s ? nB : nA;
-        const bool valid = r < nblk;
+        const int qi = qrow_of(r);
+        const bool valid = qi >= 0;
         const bool warp_valid = __any_sync(0xffffffffu, valid);
-        const int grow = row0 + (valid ? r : 0);
+        const int grow = row0 + max(qi, 0);
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + kSCol + s * 128, tO = tmem + lane_off + s * kOCol;
         const uint64_t* mrow = a.mask + (size_t)(grow / G) * a.W;
@@ -1002,8 +1025,9 @@ __global__ void __launch_bounds__(kDualThreads, 1) tree_attn_dual_kernel(
     }
     __syncthreads();
     if (warp < kDualSoftmaxWarps && ntiles > 0) {
-        const bool valid = r < nblk;
-        const int grow = row0 + (valid ? r : 0);
+        const int qi = qrow_of(r);
+        const bool valid = qi >= 0;
+        const int grow = row0 + max(qi, 0);
         const int node = grow / G, hq = hk * G + grow % G;
         float* dst = a.out + (((size_t)b * N + node) * a.Hq + hq) * D + strm * (D / 2);
         if (bad) {
@@ -1194,8 +1218,8 @@ int launch_bf16(AttnArgs& a, const AttnPlan& p, cudaStream_t st) {
     } else {
         tmq = tmk;  // unused
     }
-    if (p.S == 1 && !a.spread && (size_t)DualSmem<D>::kBytes <= (size_t)max_smem_optin()) {
-        // blocks of more than 64 rows with unsplit keys: two streams per CTA
+    if (p.S == 1 && (size_t)DualSmem<D>::kBytes <= (size_t)max_smem_optin()) {
+        // keys not split: two streams per CTA
         auto kern = tree_attn_dual_kernel<D>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DualSmem<D>::kBytes);
         cudaLaunchConfig_t cfg = {};
