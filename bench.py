@@ -324,14 +324,15 @@ def run_e2e(step, steps, warmup, pipelined=True):
     input (h, q, verifier logits, tree hidden states, the tree's K/V rows)
     travels in one packed host-to-device copy and the results in one packed
     read; the tree's K/V rows then move from the staging buffer into their
-    cache slots on the device.  The copy and the step (its K/V placement, five
-    calls and result read) are CUDA graphs.
+    cache slots on the device.  The input copy, the step (its K/V placement and
+    five calls) and the result read are CUDA graphs on three streams.
 
-    pipelined: two staging buffers; step k + 1's inputs are copied on a copy
-    stream while step k computes, and the host waits for step k's results
-    right after enqueuing step k + 1 (two steps in flight, as a serving loop
-    with a prefetching input queue runs).  Otherwise every step copies, computes
-    and is waited for before the next starts."""
+    pipelined: two staging and two result buffers; step k + 1's inputs are
+    copied while step k computes, step k's results are read back while step
+    k + 1 computes, and the host waits for step k's results right after
+    enqueuing step k + 1 (two steps in flight, as a serving loop with a
+    prefetching input queue runs).  Otherwise every step copies, computes, is
+    read back and waited for before the next starts."""
     torch = step.torch
     L = int(step.kv_len0[0].item())
     N = step.N
@@ -343,13 +344,10 @@ def run_e2e(step, steps, warmup, pipelined=True):
     staged = [_pack(src, dev) for _ in range(nbuf)]  # (device buffer, views) per slot
     hbuf_in, _ = _pack([t.cpu() for t in src], "cpu", pinned=True)
     names_out = ("accept_len", "best_node", "path_nodes", "next_tok")
-    dbuf_out, outs = _pack([step.acc[n] for n in names_out] + [step.h_next], dev)
-    for n, v in zip(names_out, outs[:4]):
-        step.acc[n] = v
-    step.h_next = outs[4]
-    hbuf_out = [torch.empty(dbuf_out.numel(), dtype=torch.uint8).pin_memory() for _ in range(nbuf)]
+    results = [_pack([step.acc[n] for n in names_out] + [step.h_next], dev) for _ in range(nbuf)]
+    hbuf_out = [torch.empty(results[0][0].numel(), dtype=torch.uint8).pin_memory() for _ in range(nbuf)]
     h2d = hbuf_in.numel()
-    d2h = dbuf_out.numel()
+    d2h = results[0][0].numel()
 
     def enqueue_copy(p):
         staged[p][0].copy_(hbuf_in, non_blocking=True)
@@ -358,45 +356,58 @@ def run_e2e(step, steps, warmup, pipelined=True):
         views = staged[p][1]
         for n, v in zip(names_in, views):
             setattr(step, n, v)
+        outs = results[p][1]
+        for n, v in zip(names_out, outs[:4]):
+            step.acc[n] = v
+        step.h_next = outs[4]
         step.kc[:, :, L:L + N].copy_(views[4])
         step.vc[:, :, L:L + N].copy_(views[5])
         step.run()
-        hbuf_out[p].copy_(dbuf_out, non_blocking=True)
 
-    cs, ss = torch.cuda.Stream(), torch.cuda.Stream()
-    cs.wait_stream(torch.cuda.current_stream())
-    ss.wait_stream(torch.cuda.current_stream())
+    def enqueue_read(p):
+        hbuf_out[p].copy_(results[p][0], non_blocking=True)
+
+    cs, ss, rs = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    for x in (cs, ss, rs):
+        x.wait_stream(torch.cuda.current_stream())
     for p in range(nbuf):  # warm-up before capture
         with torch.cuda.stream(cs):
             enqueue_copy(p)
         ss.wait_stream(cs)
         with torch.cuda.stream(ss):
             enqueue_step(p)
+        rs.wait_stream(ss)
+        with torch.cuda.stream(rs):
+            enqueue_read(p)
     torch.cuda.synchronize()
-    gc, gs = [], []
+    gc, gs, gr = [], [], []
     for p in range(nbuf):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cs):
-            enqueue_copy(p)
-        gc.append(g)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=ss):
-            enqueue_step(p)
-        gs.append(g)
+        for lst, strm, fn in ((gc, cs, enqueue_copy), (gs, ss, enqueue_step), (gr, rs, enqueue_read)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=strm):
+                fn(p)
+            lst.append(g)
     copied = [torch.cuda.Event() for _ in range(nbuf)]
+    computed = [torch.cuda.Event() for _ in range(nbuf)]
     done = [torch.cuda.Event() for _ in range(nbuf)]
 
     def launch(k):
         p = k % nbuf
         with torch.cuda.stream(cs):
             if k >= nbuf:
-                cs.wait_event(done[p])  # slot p was read by step k - nbuf
+                cs.wait_event(computed[p])  # slot p's inputs were read by step k - nbuf
             gc[p].replay()
             copied[p].record(cs)
         with torch.cuda.stream(ss):
             ss.wait_event(copied[p])
+            if k >= nbuf:
+                ss.wait_event(done[p])  # slot p's results of step k - nbuf are on the host
             gs[p].replay()
-            done[p].record(ss)
+            computed[p].record(ss)
+        with torch.cuda.stream(rs):
+            rs.wait_event(computed[p])
+            gr[p].replay()
+            done[p].record(rs)
 
     def run(n):
         for k in range(n):
@@ -1376,8 +1387,8 @@ def main():
             "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "pipeline": "two steps in flight: the next step's inputs are copied from pinned host "
-                                "memory on a copy stream while the current step computes; every step's "
-                                "results are read back and waited for by the host"},
+                                "memory and the previous step's results read back on streams of their own "
+                                "while the current step computes; the host waits for every step's results"},
             "e2e_serial": {"value": world * ke / e2e_serial_s, "unit": "steps/s",
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": step.launches * K}
