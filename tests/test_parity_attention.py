@@ -54,6 +54,11 @@ def _run(M, x, kv_len, t, scale):
     ("c1", 1, 8, 2, 128, [500], 520, "bf16"),
     ("sparse64", 1, 2, 2, 64, [1000], 1100, "bf16"),
     ("small", 1, 6, 2, 128, [4000], 4100, "bf16"),
+    # blocks of at most 64 rows with one key tile: the two-stream kernel with
+    # rows spread over the TMEM lane quarters, query heads grouped 4 (TMA
+    # query load) and 3 (rows gathered without TMA)
+    ("c1", 2, 8, 2, 64, [20, 100], 110, "bf16"),
+    ("c1", 2, 6, 2, 64, [20, 100], 110, "bf16"),
 ])
 def test_attention_full_compare(medusa, kind, B, Hq, Hkv, D, lens, Lmax, dtype):
     t = _tree(kind)
