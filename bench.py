@@ -318,7 +318,7 @@ def _pack(tensors, device, pinned=False):
     return buf, views
 
 
-def run_e2e(step, steps, warmup, pipelined=True):
+def run_e2e(step, steps, warmup, pipelined=True, host_results=False):
     """Same step through the C ABI with host buffers: per-step inputs copied from
     pinned host memory, results read back, all inside the timed region.  Every
     input (h, q, verifier logits, tree hidden states, the tree's K/V rows)
@@ -332,7 +332,10 @@ def run_e2e(step, steps, warmup, pipelined=True):
     k + 1 computes, and the host waits for step k's results right after
     enqueuing step k + 1 (two steps in flight, as a serving loop with a
     prefetching input queue runs).  Otherwise every step copies, computes, is
-    read back and waited for before the next starts."""
+    read back and waited for before the next starts.
+
+    host_results: also return, per result buffer, the read-back results as host
+    tensors (accept_len, best_node, path_nodes, next_tok, h_next)."""
     torch = step.torch
     L = int(step.kv_len0[0].item())
     N = step.N
@@ -425,6 +428,16 @@ def run_e2e(step, steps, warmup, pipelined=True):
     run(steps)
     dt = time.perf_counter() - t0
     torch.cuda.synchronize()
+    if host_results:
+        got = []
+        for p in range(nbuf):
+            base = results[p][0].data_ptr()
+            segs = []
+            for v in results[p][1]:
+                off, nb = v.data_ptr() - base, v.numel() * v.element_size()
+                segs.append(hbuf_out[p][off:off + nb].view(v.dtype).view(v.shape).clone())
+            got.append(segs)
+        return dt, h2d, d2h, got
     return dt, h2d, d2h
 
 
